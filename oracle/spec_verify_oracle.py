@@ -1,0 +1,325 @@
+"""Plain fp64 CPU oracle for batched speculative-decoding verification (accept-or-resample).
+
+TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg import this module. The GPU library never imports, links or calls it, and the two share no code.
+
+What it computes, and where the pages define it (page title, then section):
+
+* [R] "Speculative decoding", rayaq.ca ml-models:
+  - Mechanics, One round, steps 3-5: left-to-right accept while u < min(1, p(x)/q(x)); on the first
+    rejection a replacement drawn from max(0, p - q) / sum max(0, p - q); a bonus token from p at
+    position gamma + 1 when every draft survives.
+  - Why the output is exactly the target's: alpha = sum_x min(p(x), q(x)); temperature applied to
+    both p and q before the test.
+  - The greedy case: keep drafts while they equal the target's argmax, replace the first mismatch by
+    the argmax, add the bonus argmax when all match.
+  - Implementation: p rows = softmax(target logits / temp), q rows = softmax(draft logits / temp).
+* [B] "Inference: distillation and speculative decoding", brunomaga.github.io:
+  - Draft-model speculative decoding: the same two rules (that page names the draft distribution p
+    and the target q; this module uses p = target, q = draft throughout).
+  - Knowledge distillation: the temperature softmax.
+* [C] "Speculative decoding", cgnarendiran.github.io blog, The correction that makes it exact:
+  the accept probability and the normalised residual.
+
+Parity status: every function below is pinned by the tests in ``tests/test_oracle.py`` and
+``tests/test_montecarlo.py`` (page-printed worked examples, closed forms, identities, an exact
+rational-arithmetic restatement and Monte-Carlo statistics). No function here is "parity unpinned".
+
+Readings where the pages leave a step open (each repeated in the design notes):
+
+* Which uniform drives what: ``u[b, i]`` (i < gamma_b) the accept test at position i, ``u[b, G]``
+  the residual draw, ``u[b, G + 1]`` the bonus draw, with G = gamma_max (fixed columns).
+* The library draw (torch.multinomial) is replaced by an inverse CDF in index order with a strict
+  ``>``: token j = min{ j : sum_{v <= j} w_v > u * sum_v w_v }. Zero-weight tokens are never chosen.
+  If rounding leaves no prefix above the threshold, the last token with w > 0 is taken.
+* A residual with zero total mass at a rejection (impossible in exact arithmetic) falls back to a
+  bonus-style draw from that position's p with ``u[b, G]``.
+* q(x) = 0 for a drafted x gives ratio 1 (accept).
+* Greedy rows are the rows with temperature exactly 0. Argmax ties go to the lowest index. Greedy
+  alpha_i = [x_i == g_i], p(x_i) = [x_i == g_i], q(x_i) = 1 (one-hot p and one-hot drafter).
+* alpha_i, p_i(x_i), q_i(x_i) are reported for every i < gamma_b, also after the first rejection;
+  0 for padding positions i >= gamma_b.
+* The bonus row of row b is target position gamma_b (ragged lengths), not gamma_max.
+* Row errors (all outputs of the row -1 / 0): draft_len outside [0, G]; temperature NaN, negative,
+  infinite or in (0, FLT_MIN); a drafted token outside [0, V) at i < gamma_b; for sampled rows a
+  used uniform outside [0, 1); a read logit row holding NaN or +inf, or holding only -inf.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+MARGIN = 1e-5           # decision margin of the parity rule (absolute on u, relative on the CDF)
+FLT_MIN = np.float64(np.finfo(np.float32).tiny)   # smallest normal fp32, lower bound of a sampled T
+
+
+# ----------------------------------------------------------------------------------------------
+# Single-position building blocks
+# ----------------------------------------------------------------------------------------------
+
+def temperature_softmax(z, T):
+    """softmax(z / T) in fp64 ([R] Implementation: softmax of logits / temp for both models;
+    [B] Knowledge distillation: the temperature softmax). The stored logits widen to fp64 exactly.
+    -inf logits get probability 0."""
+    y = np.asarray(z, dtype=np.float64) / np.float64(T)
+    m = np.max(y)
+    e = np.exp(y - m)
+    return e / np.sum(e)
+
+
+def accept_ratio(p_x, q_x):
+    """min(1, p(x)/q(x)) ([R] One round, step 3; [C] The correction that makes it exact).
+    q(x) = 0 reads as ratio 1: a token the drafter proposed with zero mass is kept."""
+    if q_x <= 0.0:
+        return 1.0
+    return min(1.0, p_x / q_x)
+
+
+def residual_weights(p, q):
+    """max(0, p - q), unnormalised ([R] One round, step 4; [C] residual numerator)."""
+    return np.maximum(0.0, p - q)
+
+
+def inverse_cdf(w, u):
+    """Token j = min{ j : sum_{v <= j} w_v > u * W } with W the running total at the end; index
+    order, strict '>'. Stands in for the pages' library draw from the normalised weights w / W
+    ([R] Implementation, torch.multinomial). Overrun by rounding takes the last token with w > 0."""
+    c = np.cumsum(w)
+    t = u * c[-1]
+    hit = np.flatnonzero(c > t)
+    if hit.size:
+        return int(hit[0])
+    return int(np.flatnonzero(w > 0)[-1])
+
+
+def admissible_draws(w, u, eps=MARGIN):
+    """Every token whose CDF interval [C_{j-1}, C_j] comes within eps * W of the threshold u * W.
+    The draw is fixed (a single admissible token) when the threshold is farther than eps * W from
+    every interval boundary. Returns (sorted token list, gap), gap = distance of the threshold to the
+    nearest boundary of the chosen token's interval, divided by W."""
+    c = np.cumsum(w)
+    W = c[-1]
+    t = u * W
+    lo = np.concatenate(([0.0], c[:-1]))
+    adm = np.flatnonzero((lo <= t + eps * W) & (c >= t - eps * W))
+    j = inverse_cdf(w, u)
+    gap = min(t - lo[j], c[j] - t) / W if W > 0 else 0.0
+    last_pos = int(np.flatnonzero(w > 0)[-1])
+    toks = set(int(a) for a in adm)
+    if t >= W - eps * W:           # the overrun rule may apply within the margin
+        toks.add(last_pos)
+    toks.add(j)
+    return sorted(toks), gap
+
+
+def greedy_argmax(z):
+    """Target argmax on the stored logits, lowest index on ties ([B] Draft-model speculative decoding,
+    greedy rule; [R] The greedy case)."""
+    return int(np.argmax(np.asarray(z, dtype=np.float64)))
+
+
+# ----------------------------------------------------------------------------------------------
+# Row validity (host-visible data errors)
+# ----------------------------------------------------------------------------------------------
+
+def _bad_logits(z):
+    z = np.asarray(z, dtype=np.float64)
+    return bool(np.any(np.isnan(z)) or np.any(z == np.inf) or np.all(z == -np.inf))
+
+
+def row_is_valid(zt, zd, x, gamma_b, T, u, G, V):
+    """Applies the row-error rules listed in the module docstring. zt: [G+1, V], zd: [G, V]."""
+    if not (0 <= gamma_b <= G):
+        return False
+    T = np.float64(T)
+    if np.isnan(T) or T < 0 or np.isinf(T) or (0 < T < FLT_MIN):
+        return False
+    greedy = T == 0
+    for i in range(gamma_b):
+        if not (0 <= int(x[i]) < V):
+            return False
+    if not greedy:
+        used = [u[i] for i in range(gamma_b)] + [u[G], u[G + 1]]
+        for uu in used:
+            uu = np.float64(uu)
+            if not (0.0 <= uu < 1.0):
+                return False
+    for i in range(gamma_b + 1):
+        if _bad_logits(zt[i]):
+            return False
+    if not greedy:
+        for i in range(gamma_b):
+            if _bad_logits(zd[i]):
+                return False
+    return True
+
+
+# ----------------------------------------------------------------------------------------------
+# One row
+# ----------------------------------------------------------------------------------------------
+
+@dataclass
+class RowResult:
+    tokens: list            # emitted tokens (k accepted drafts + one correction or bonus), or [] on error
+    k: int                  # accepted drafts, -1 on error
+    alpha: np.ndarray       # [G]
+    p_draft: np.ndarray     # [G]
+    q_draft: np.ndarray     # [G]
+    valid: bool = True
+    greedy: bool = False
+    ratio: np.ndarray = None        # [gamma_b] min(1, p/q) (sampled rows)
+    margin: np.ndarray = None       # [gamma_b] |u_i - r_i| (sampled rows)
+    outcomes: dict = field(default_factory=dict)   # legit k -> admissible final tokens (diagnostics)
+    exact: bool = True              # True when the only legit outcome is (k, tokens[-1])
+    final_gap: float = 1.0
+
+
+def verify_row(zt, zd, x, gamma_b, T, u, G, diagnostics=False, eps=MARGIN):
+    """One row of the batch: the round's verification half ([R] One round steps 3-5 and
+    Implementation, after the target pass; [R] The greedy case for T == 0).
+
+    zt: [G+1, V] target logits, zd: [G, V] draft logits, x: [G] drafted tokens, u: [G+2] uniforms.
+    """
+    V = np.asarray(zt).shape[-1]
+    alpha = np.zeros(G)
+    pd = np.zeros(G)
+    qd = np.zeros(G)
+    if not row_is_valid(zt, zd, x, gamma_b, T, u, G, V):
+        return RowResult([], -1, alpha, pd, qd, valid=False)
+
+    if np.float64(T) == 0.0:
+        # Greedy: keep drafts while they equal the target argmax; the correction or bonus is the argmax.
+        g = [greedy_argmax(zt[i]) for i in range(gamma_b + 1)]
+        for i in range(gamma_b):
+            hit = int(x[i]) == g[i]
+            alpha[i] = 1.0 if hit else 0.0
+            pd[i] = 1.0 if hit else 0.0
+            qd[i] = 1.0
+        k = 0
+        while k < gamma_b and int(x[k]) == g[k]:
+            k += 1
+        toks = [int(x[i]) for i in range(k)] + [g[k]]
+        res = RowResult(toks, k, alpha, pd, qd, greedy=True)
+        res.outcomes = {k: [g[k]]}
+        return res
+
+    # Sampled row. Target p_i and draft q_i at every verified position i < gamma_b, alpha_i for each.
+    ratio = np.zeros(gamma_b)
+    margin = np.zeros(gamma_b)
+    p_rows, q_rows = [], []
+    for i in range(gamma_b):
+        p = temperature_softmax(zt[i], T)
+        q = temperature_softmax(zd[i], T)
+        p_rows.append(p)
+        q_rows.append(q)
+        xi = int(x[i])
+        pd[i], qd[i] = p[xi], q[xi]
+        alpha[i] = np.sum(np.minimum(p, q))          # [R] Why the output is exactly the target's
+        ratio[i] = accept_ratio(p[xi], q[xi])
+        margin[i] = abs(np.float64(u[i]) - ratio[i])
+
+    # Accept left to right, stop at the first rejection ([R] One round, step 3).
+    k = 0
+    while k < gamma_b and np.float64(u[k]) < ratio[k]:
+        k += 1
+
+    def final_draw(kk):
+        """The token after kk accepted drafts, and its weights and uniform."""
+        if kk < gamma_b:
+            w = residual_weights(p_rows[kk], q_rows[kk])      # [R] One round, step 4
+            uu = np.float64(u[G])
+            if not np.sum(w) > 0.0:                           # zero residual mass: draw from p
+                w = p_rows[kk]
+        else:
+            w = temperature_softmax(zt[gamma_b], T)            # [R] One round, step 5 (bonus)
+            uu = np.float64(u[G + 1])
+        return w, uu
+
+    w, uu = final_draw(k)
+    j = inverse_cdf(w, uu)
+    res = RowResult([int(x[i]) for i in range(k)] + [j], k, alpha, pd, qd,
+                    ratio=ratio, margin=margin)
+    if diagnostics:
+        # Every accept count reachable when decisions within eps of their threshold may go either way,
+        # and for each the tokens whose CDF interval lies within eps of the draw's threshold.
+        legit = []
+        for kk in range(gamma_b + 1):
+            if all(np.float64(u[i]) < ratio[i] + eps for i in range(kk)) and \
+                    (kk == gamma_b or np.float64(u[kk]) >= ratio[kk] - eps):
+                legit.append(kk)
+        for kk in legit:
+            ww, uk = final_draw(kk)
+            adm, gap = admissible_draws(ww, uk, eps)
+            res.outcomes[kk] = adm
+            if kk == k:
+                res.final_gap = gap
+        res.exact = legit == [k] and res.outcomes[k] == [j]
+    return res
+
+
+# ----------------------------------------------------------------------------------------------
+# The batch
+# ----------------------------------------------------------------------------------------------
+
+@dataclass
+class BatchResult:
+    out_tokens: np.ndarray       # [B, G+1] int32, -1 padding
+    out_num_emitted: np.ndarray  # [B] int32, k+1 or -1
+    out_alpha: np.ndarray        # [B, G] fp64
+    out_p_draft: np.ndarray      # [B, G] fp64
+    out_q_draft: np.ndarray      # [B, G] fp64
+    rows: list                   # RowResult per row (diagnostics)
+
+
+def oracle_verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                  rows=None, diagnostics=False, eps=MARGIN):
+    """Batched verification, one row at a time in plain loops.
+
+    target_logits [B, G+1, V], draft_logits [B, G, V] (any float dtype holding the stored values),
+    draft_tokens [B, G] int, draft_len [B] int or None (all G), temperature [B] fp32 (0 = greedy),
+    uniforms [B, G+2] fp32. ``rows`` restricts the work to a subset of rows (others stay -1).
+    """
+    target_logits = np.asarray(target_logits)
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    if draft_len is None:
+        draft_len = np.full(B, G, dtype=np.int64)
+    out_tokens = np.full((B, G + 1), -1, dtype=np.int32)
+    out_num = np.full(B, -1, dtype=np.int32)
+    out_alpha = np.zeros((B, G))
+    out_p = np.zeros((B, G))
+    out_q = np.zeros((B, G))
+    results = [None] * B
+    for b in (range(B) if rows is None else rows):
+        zd = draft_logits[b] if draft_logits is not None else np.zeros((G, V))
+        r = verify_row(target_logits[b], zd, draft_tokens[b], int(draft_len[b]),
+                       np.float32(temperature[b]), uniforms[b], G, diagnostics=diagnostics, eps=eps)
+        results[b] = r
+        if r.valid:
+            out_tokens[b, :len(r.tokens)] = r.tokens
+            out_num[b] = len(r.tokens)
+            out_alpha[b] = r.alpha
+            out_p[b] = r.p_draft
+            out_q[b] = r.q_draft
+    return BatchResult(out_tokens, out_num, out_alpha, out_p, out_q, results)
+
+
+# ----------------------------------------------------------------------------------------------
+# Drafting helper (input preparation for the small configuration, not the verification path)
+# ----------------------------------------------------------------------------------------------
+
+def sample_drafts(draft_logits, temperature, uniforms):
+    """Draft tokens x_i ~ q_i by inverse CDF in fp64 ([R] One round, step 1: x_i ~ q). Greedy rows
+    (T == 0) take the draft argmax ([B] DraftModel: greedy drafter). uniforms: [B, G] fp32."""
+    draft_logits = np.asarray(draft_logits)
+    B, G, V = draft_logits.shape
+    x = np.zeros((B, G), dtype=np.int32)
+    for b in range(B):
+        for i in range(G):
+            if np.float64(temperature[b]) == 0.0:
+                x[b, i] = greedy_argmax(draft_logits[b, i])
+            else:
+                x[b, i] = inverse_cdf(temperature_softmax(draft_logits[b, i], temperature[b]),
+                                      np.float64(uniforms[b, i]))
+    return x
