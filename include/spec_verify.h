@@ -1,0 +1,131 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) batched speculative-decoding verifier.
+ *
+ * The operation (accept-or-resample verification of drafted tokens) is the one defined on these
+ * pages, cited by page title and section:
+ *   [R] "Speculative decoding", rayaq.ca ml-models -- Mechanics, One round, steps 2-5 (accept left to
+ *       right while u < min(1, p(x)/q(x)); replacement from max(0, p - q) / sum max(0, p - q) at the
+ *       first rejection; bonus token from p at position gamma + 1 when every draft survives);
+ *       Why the output is exactly the target's (alpha = sum_x min(p, q); the same temperature on p and
+ *       q); The greedy case (argmax-prefix match, argmax correction and bonus); Implementation (p and q
+ *       rows are softmax(logits / temp)).
+ *   [B] "Inference: distillation and speculative decoding", brunomaga.github.io -- Draft-model
+ *       speculative decoding (the greedy and the sampled acceptance rules; batched rows accept
+ *       different counts, so lengths are tracked per row).
+ *   [C] "Speculative decoding", cgnarendiran.github.io blog -- The correction that makes it exact.
+ * Throughout, p is the TARGET distribution and q the DRAFT distribution (page [B] swaps the names).
+ *
+ * Shapes: B rows, G = gamma_max padded draft width, V vocabulary, s = element size of the logits.
+ * Row b verifies gamma_b = draft_len[b] drafted tokens (0 <= gamma_b <= G). All tensors are dense,
+ * row-major, contiguous.
+ *
+ * Sampling rule used for the library draws of the pages: inverse CDF in vocabulary-index order with
+ * a strict '>' against u times the running total; tokens with zero weight are never chosen; if
+ * rounding leaves no prefix above the threshold, the last token with positive weight is taken. A
+ * rejection whose residual has zero total mass (possible only through rounding) draws from that
+ * position's p with the residual uniform instead.
+ *
+ * Uniforms: u[b, i] (i < gamma_b) drives the accept test at position i, u[b, G] the residual draw,
+ * u[b, G + 1] the bonus draw. Greedy rows (temperature exactly 0) read no uniforms and no draft
+ * logits.
+ *
+ * Ownership: every pointer is caller-owned CUDA device memory (or host memory the device can address
+ * directly). The library allocates nothing and holds no per-call state; all per-call scratch lives
+ * in the caller's workspace.
+ *
+ * Asynchrony: calls validate their arguments on the host, enqueue work on `cuda_stream` (NULL = the
+ * legacy default stream) and return. Outputs are valid once that stream has been synchronised.
+ *
+ * Errors: argument errors return a nonzero sv_status synchronously and enqueue nothing. Launch
+ * errors return SV_ERR_CUDA. Data errors never trap: they mark the row (out_num_emitted[b] = -1,
+ * out_tokens[b, :] = -1, out_alpha/p/q[b, :] = 0). Row data errors are: draft_len outside [0, G];
+ * temperature NaN, negative, infinite or in (0, FLT_MIN); a drafted token outside [0, V) at
+ * i < gamma_b; for sampled rows a used uniform outside [0, 1); a read logit row holding NaN or +inf,
+ * or holding only -inf.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_NULL_POINTER = 1,        /* a required pointer is NULL                                   */
+  SV_ERR_BAD_SHAPE = 2,           /* B < 1, gamma_max outside [0, SV_MAX_GAMMA], V < 1, V too large
+                                     for one thread-block cluster, or the launch grid overflows    */
+  SV_ERR_BAD_DTYPE = 3,           /* dtype is not an sv_dtype                                     */
+  SV_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < spec_verify_workspace_size(...), or NULL   */
+  SV_ERR_MISALIGNED = 5,          /* a pointer is not aligned to its element type (workspace: 16 B) */
+  SV_ERR_CUDA = 6,                /* a CUDA runtime call failed (device query or launch)          */
+  SV_ERR_UNSUPPORTED_DEVICE = 7   /* the current device is not compute capability 10.3           */
+} sv_status;
+
+typedef enum { SV_DTYPE_F32 = 0, SV_DTYPE_BF16 = 1 } sv_dtype;
+
+#define SV_MAX_GAMMA 64
+#define SV_VERSION 1
+
+/* Bytes of device workspace spec_verify needs for these sizes (per-position records and one arrival
+ * counter per row), a multiple of 256. Returns 0 for invalid sizes.
+ *
+ * The workspace must hold zeros before its first use (e.g. one cudaMemset after allocation). Every
+ * call that runs to completion leaves it zeroed again, so it can be reused without clearing. One
+ * workspace serves one call at a time: two calls in flight on the same workspace race. */
+size_t spec_verify_workspace_size(int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
+
+/* Batched verification of one speculative round ([R] One round, steps 3-5; [R] The greedy case).
+ *
+ * target_logits   [B, G+1, V] dtype   target logits; row (b, i) gives p_{b,i} = softmax(z / T_b).
+ *                                     Rows i > gamma_b are never read.
+ * draft_logits    [B, G, V]   dtype   draft logits; q_{b,i} = softmax(z / T_b). Rows i >= gamma_b and
+ *                                     all rows of greedy rows are never read. May be NULL if G == 0.
+ * draft_tokens    [B, G]      int32   drafted tokens x_{b,i}; entries i >= gamma_b are ignored.
+ * draft_len       [B]         int32   gamma_b in [0, G]; NULL means every row has gamma_b = G.
+ * temperature     [B]         fp32    T_b; 0 selects greedy verification, > 0 sampled verification.
+ * uniforms        [B, G+2]    fp32    caller-drawn uniforms in [0, 1) (layout above).
+ * out_tokens      [B, G+1]    int32   emitted tokens: gamma accepted drafts, then the correction or
+ *                                     bonus token, then -1 padding.
+ * out_num_emitted [B]         int32   k_b + 1 in [1, gamma_b + 1]; -1 marks a row data error.
+ * out_alpha       [B, G]      fp32    alpha_{b,i} = sum_v min(p_{b,i}(v), q_{b,i}(v)) for i < gamma_b
+ *                                     (every verified position, also after the first rejection;
+ *                                     greedy rows: 1 if x_i is the target argmax, else 0); 0 for
+ *                                     i >= gamma_b. May be NULL.
+ * B, gamma_max, V, dtype              sizes and the sv_dtype of both logit tensors.
+ * workspace, workspace_bytes          zero-initialised device scratch of at least
+ *                                     spec_verify_workspace_size(B, gamma_max, V, dtype) bytes,
+ *                                     16-byte aligned.
+ * cuda_stream                         a cudaStream_t, or NULL.
+ * Returns an sv_status. */
+int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                const int32_t* draft_len, const float* temperature, const float* uniforms,
+                int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* spec_verify with two more outputs, for probability-level checks:
+ * out_p_draft [B, G] fp32  p_{b,i}(x_{b,i}) (greedy rows: 1 if x_i is the target argmax, else 0);
+ * out_q_draft [B, G] fp32  q_{b,i}(x_{b,i}) (greedy rows: 1); both 0 for i >= gamma_b.
+ * Either may be NULL. Everything else is as in spec_verify. */
+int spec_verify_ex(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                   const int32_t* draft_len, const float* temperature, const float* uniforms,
+                   int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                   float* out_p_draft, float* out_q_draft,
+                   int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                   void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Static description of an sv_status value (never NULL). */
+const char* spec_verify_status_string(int status);
+
+/* SV_VERSION of the built library. */
+int spec_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,188 @@
+"""ctypes binding of libspecverify.so: the C ABI in include/spec_verify.h under the same names.
+
+Argument marshalling only: every step of the verification runs in the library's CUDA kernels.
+Torch tensors supply device memory and the stream. There is no CPU fallback: if the library is not
+built, importing the functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from .build import LIB_PATH
+
+SV_OK = 0
+SV_DTYPE_F32 = 0
+SV_DTYPE_BF16 = 1
+SV_MAX_GAMMA = 64
+
+STATUS_NAMES = {
+    0: "SV_OK", 1: "SV_ERR_NULL_POINTER", 2: "SV_ERR_BAD_SHAPE", 3: "SV_ERR_BAD_DTYPE",
+    4: "SV_ERR_WORKSPACE_TOO_SMALL", 5: "SV_ERR_MISALIGNED", 6: "SV_ERR_CUDA",
+    7: "SV_ERR_UNSUPPORTED_DEVICE",
+}
+
+EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
+            "spec_verify_status_string", "spec_verify_version")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str = "spec_verify"):
+        self.status = status
+        super().__init__(f"{where} returned {status} ({spec_verify_status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not LIB_PATH.exists():
+                raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(str(LIB_PATH))
+            vp, i32, f32p, i32p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p
+            common = [vp, vp, i32p, i32p, f32p, f32p, i32p, i32p, f32p]
+            tail = [i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
+            L.spec_verify.argtypes = common + tail
+            L.spec_verify.restype = ctypes.c_int
+            L.spec_verify_ex.argtypes = common + [f32p, f32p] + tail
+            L.spec_verify_ex.restype = ctypes.c_int
+            L.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
+            L.spec_verify_workspace_size.restype = ctypes.c_size_t
+            L.spec_verify_status_string.argtypes = [ctypes.c_int]
+            L.spec_verify_status_string.restype = ctypes.c_char_p
+            L.spec_verify_version.argtypes = []
+            L.spec_verify_version.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def spec_verify_workspace_size(B: int, gamma_max: int, V: int, dtype: int) -> int:
+    return int(lib().spec_verify_workspace_size(B, gamma_max, V, dtype))
+
+
+def spec_verify_status_string(status: int) -> str:
+    return lib().spec_verify_status_string(int(status)).decode()
+
+
+def spec_verify_version() -> int:
+    return int(lib().spec_verify_version())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SV_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return SV_DTYPE_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check(t, name, dtype=None, shape=None, device=None):
+    if t is None:
+        return
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                   out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft,
+                   workspace, stream=None) -> None:
+    """Calls the C ABI spec_verify_ex on torch tensors (shapes from target_logits [B, G+1, V]).
+    Raises SpecVerifyError on a nonzero status."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    _check(target_logits, "target_logits", device=dev)
+    _check(draft_logits, "draft_logits", dtype=target_logits.dtype, shape=(B, G, V), device=dev)
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, G), dev)
+    _check(draft_len, "draft_len", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, G + 2), dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B, G + 1), dev)
+    _check(out_num_emitted, "out_num_emitted", torch.int32, (B,), dev)
+    for name, t in (("out_alpha", out_alpha), ("out_p_draft", out_p_draft),
+                    ("out_q_draft", out_q_draft)):
+        _check(t, name, torch.float32, (B, G), dev)
+    _check(workspace, "workspace", device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().spec_verify_ex(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
+        _ptr(temperature), _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted),
+        _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
+        B, G, V, _dtype_code(target_logits), _ptr(workspace), ws_bytes,
+        _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_ex")
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                out_tokens, out_num_emitted, out_alpha, workspace, stream=None) -> None:
+    """Calls the C ABI spec_verify on torch tensors (see spec_verify_ex)."""
+    spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                   out_tokens, out_num_emitted, out_alpha, None, None, workspace, stream)
+
+
+_ws_cache = {}
+
+
+def workspace_for(B, G, V, dtype_code, device, stream=None):
+    """A zero-initialised workspace cached per (device, stream), grown on demand. Calls leave it
+    zeroed, so it is reused without clearing; it must not serve two calls in flight at once."""
+    import torch
+    need = spec_verify_workspace_size(B, G, V, dtype_code)
+    key = (str(device), _stream_handle(stream, device))
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+           with_probs=False, stream=None):
+    """Allocates the outputs, runs spec_verify(_ex) and returns
+    (out_tokens [B, G+1], out_num_emitted [B], out_alpha [B, G][, out_p, out_q])."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    out_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    out_alpha = torch.empty((B, G), dtype=torch.float32, device=dev)
+    out_p = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
+    out_q = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
+    ws = workspace_for(B, G, V, _dtype_code(target_logits), dev, stream)
+    spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                   out_tokens, out_num, out_alpha, out_p, out_q, ws, stream)
+    if with_probs:
+        return out_tokens, out_num, out_alpha, out_p, out_q
+    return out_tokens, out_num, out_alpha

@@ -1,0 +1,104 @@
+"""The C-ABI library builds, loads, exports every function include/spec_verify.h declares, and rejects
+bad arguments on the host before touching the GPU. CPU only: no compute call is made."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "spec_verify.h"
+
+
+@pytest.fixture(scope="module")
+def L():
+    import speculative_decoding_verification_55_gb300 as m
+    m.build_library()
+    return m.lib()
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_verify\w*)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for n in ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
+              "spec_verify_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    import speculative_decoding_verification_55_gb300 as m
+    for name in declared_functions():
+        assert callable(getattr(m, name)), name
+
+
+def test_version_and_status_strings(L):
+    import speculative_decoding_verification_55_gb300 as m
+    assert m.spec_verify_version() == 1
+    for code in range(8):
+        s = m.spec_verify_status_string(code)
+        assert s.startswith("SV_")
+    assert "unknown" in m.spec_verify_status_string(99)
+
+
+def test_workspace_size(L):
+    import speculative_decoding_verification_55_gb300 as m
+    for B, G in ((1, 0), (1, 4), (8, 4), (1024, 8), (7, 64)):
+        n = m.spec_verify_workspace_size(B, G, 32000, 1)
+        assert n % 256 == 0 and n >= 8 * B * (G + 1) + 4 * B
+    assert m.spec_verify_workspace_size(0, 4, 100, 0) == 0
+    assert m.spec_verify_workspace_size(2, 65, 100, 0) == 0
+    assert m.spec_verify_workspace_size(2, -1, 100, 0) == 0
+    assert m.spec_verify_workspace_size(2, 4, 0, 0) == 0
+    assert m.spec_verify_workspace_size(2, 4, 100, 7) == 0
+
+
+FAKE = 0x7f0000000000   # never dereferenced: every case below fails validation first
+
+
+def call(L, **kw):
+    B, G, V, dtype = kw.get("B", 2), kw.get("G", 3), kw.get("V", 256), kw.get("dtype", 1)
+    args = dict(zt=FAKE, zd=FAKE + 4096, tok=FAKE + 8192, dl=FAKE + 12288, T=FAKE + 16384,
+                u=FAKE + 20480, ot=FAKE + 24576, on=FAKE + 28672, oa=FAKE + 32768,
+                ws=FAKE + 65536, wsb=1 << 20)
+    args.update({k: v for k, v in kw.items() if k in args})
+    return L.spec_verify(args["zt"], args["zd"], args["tok"], args["dl"], args["T"], args["u"],
+                         args["ot"], args["on"], args["oa"], B, G, V, dtype, args["ws"],
+                         args["wsb"], None)
+
+
+def test_argument_errors_are_host_side(L):
+    assert call(L, dtype=5) == 3                      # SV_ERR_BAD_DTYPE
+    assert call(L, B=0) == 2                          # SV_ERR_BAD_SHAPE
+    assert call(L, G=65) == 2
+    assert call(L, V=0) == 2
+    assert call(L, zt=None) == 1                      # SV_ERR_NULL_POINTER
+    assert call(L, T=None) == 1
+    assert call(L, u=None) == 1
+    assert call(L, ot=None) == 1
+    assert call(L, on=None) == 1
+    assert call(L, zd=None) == 1                      # needed when G > 0
+    assert call(L, zt=FAKE + 1) == 5                  # SV_ERR_MISALIGNED (bf16 needs 2 B)
+    assert call(L, dtype=0, zt=FAKE + 2) == 5         # fp32 needs 4 B
+    assert call(L, ws=FAKE + 65544) == 5              # workspace needs 16 B
+    assert call(L, ws=None) == 4                      # SV_ERR_WORKSPACE_TOO_SMALL
+    assert call(L, wsb=16) == 4
+    # V too large for one cluster: bf16 rows whose length is not a multiple of 16 bytes use the
+    # element path (at most 16 * 512 * 8 logits); vector rows at most 16 * 512 * 8 vectors.
+    assert call(L, V=65537) == 2
+    assert call(L, V=16 * 512 * 8 * 8 + 8) == 2
+    assert call(L, dtype=0, V=16 * 512 * 8 * 4 + 4) == 2
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import speculative_decoding_verification_55_gb300._binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", tmp_path / "missing.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        b.lib()
