@@ -1,0 +1,365 @@
+#!/usr/bin/env python
+"""Benchmark of batched speculative-decoding verification on GB300.
+
+One step = one spec_verify call over one batch of the workload: every verified position of every
+row gets its temperature softmaxes, accept test, residual or bonus draw and the row's emit.
+
+Default workload: B=1024 rows, ragged draft lengths 1..8 (gamma_max 8), V=256000 bf16 logits, 10% of
+rows greedy -- the largest of the workloads, and the one that exercises every step of the path. The
+logits (4.9 GB read per step) are far larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0). Under torchrun every rank verifies its own replica of the batch on
+its own GPU (rows are independent: weak scaling, no data-path collective); the step time is the max
+over ranks.
+
+  python bench.py [--steps K] [--warmup W] [--workload N] [--impl {gb300,reference}]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "verified positions/sec (B·(γ+1)) and logits HBM GB/s vs 8 TB/s roofline"
+UNIT = "positions/s"
+NORTH_STAR_HBM_GBS = 8000.0
+DEFAULT_WORKLOAD = 5
+TRAFFIC_FILE = ROOT / "profiles" / "sv_stream_kernel_traffic.json"
+KERNEL_SOURCES = ["sv_stream.cu", "sv_common.cuh", "sv_api.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--rows", type=int, default=0, help="use only the first N rows (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        h.update((ROOT / "speculative_decoding_verification_55_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def workload_for(args, rank):
+    from workloads import get_config, make_workload
+    import dataclasses
+    cfg = get_config(args.workload)
+    seed = cfg.seed + 1000 * rank
+    if args.rows:
+        cfg = dataclasses.replace(cfg, B=min(args.rows, cfg.B))
+    return cfg, make_workload(cfg, seed=seed, backend="torch", device="cuda")
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle, as it stands, on a bounded sample of the same workload
+# ------------------------------------------------------------------------------------------------
+
+def oracle_pool(cfg_key, seconds, seed=12345):
+    """Rows of the workload drawn on the host (numpy backend), as many as the oracle verifies in
+    about `seconds` of single-thread CPU time (calibrated on 8 rows). Input generation is untimed."""
+    import dataclasses
+
+    import numpy as np
+
+    from oracle.spec_verify_oracle import oracle_verify
+    from workloads import get_config, make_workload
+    cfg = get_config(cfg_key)
+    probe = make_workload(dataclasses.replace(cfg, B=8), seed=seed, backend="numpy")
+    t0 = time.perf_counter()
+    oracle_verify(probe.target_logits, probe.draft_logits, probe.draft_tokens, probe.draft_len,
+                  probe.temperature, probe.uniforms)
+    t8 = time.perf_counter() - t0
+    rows = int(max(8, min(cfg.B, round(seconds / max(t8, 1e-6) * 8 / 8) * 8)))
+    w = make_workload(dataclasses.replace(cfg, B=rows), seed=seed + 1, backend="numpy")
+    return w, int(np.sum(w.draft_len.astype(np.int64) + 1))
+
+
+def oracle_run(w):
+    """Wall seconds of one oracle pass over the pool's rows."""
+    from oracle.spec_verify_oracle import oracle_verify
+    t0 = time.perf_counter()
+    oracle_verify(w.target_logits, w.draft_logits, w.draft_tokens, w.draft_len, w.temperature,
+                  w.uniforms)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_rate(cfg_key, seconds):
+    """Oracle throughput (positions/s) on a bounded host-drawn sample of the workload."""
+    w, pos = oracle_pool(cfg_key, seconds)
+    secs = oracle_run(w)
+    return pos / secs, w.B, pos, secs
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(v, "1")
+    from workloads import get_config
+    cfg = get_config(args.workload)
+    per_step = 1.5      # seconds of single-thread oracle work per step
+    w, pos = oracle_pool(args.workload, per_step)
+    for _ in range(args.warmup):
+        oracle_run(w)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_run(w)
+    value = pos * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "B": cfg.B, "gamma_max": cfg.gamma_max, "V": cfg.V,
+                   "logits": cfg.dtype, "sample_rows_per_step": w.B,
+                   "sample_positions_per_step": pos},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{w.B} rows ({pos} positions) of the workload drawn on the host "
+                                   f"per step, single-thread fp64 oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import speculative_decoding_verification_55_gb300 as sv
+    sv.build_library()
+
+    cfg, w = workload_for(args, rank)
+    t = w.device_tensors(dev)
+    B, G, V = w.B, w.G, w.V
+    dcode = sv.SV_DTYPE_BF16 if cfg.dtype == "bf16" else sv.SV_DTYPE_F32
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.workspace_for(B, G, V, dcode, dev, stream)
+    out_tokens = torch.empty((B, G + 1), dtype=torch.int32, device=dev)
+    out_num = torch.empty((B,), dtype=torch.int32, device=dev)
+    out_alpha = torch.empty((B, G), dtype=torch.float32, device=dev)
+
+    def step():
+        sv.spec_verify(t["target_logits"], t["draft_logits"], t["draft_tokens"], t["draft_len"],
+                       t["temperature"], t["uniforms"], out_tokens, out_num, out_alpha, ws, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    clock_info = clocks.stop()
+    ms_step = ms_total / args.steps
+    if world > 1:
+        mt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(mt.item())
+    positions = w.positions()
+    value = positions * world / (ms_step * 1e-3)
+    algo_bytes = w.algorithmic_bytes()
+    achieved_gbs = algo_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    traffic = None
+    if TRAFFIC_FILE.exists():
+        tr = json.loads(TRAFFIC_FILE.read_text())
+        if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == cfg.name:
+            traffic = tr["bytes_per_full_launch"]
+
+    # ---- end to end: pinned host inputs -> device, the call, outputs -> pinned host ----
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in t.items()}
+        dev_in = {k: torch.empty_like(v) for k, v in t.items()}
+        h_tok = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
+        h_num = torch.empty((B,), dtype=torch.int32).pin_memory()
+        h_alpha = torch.empty((B, G), dtype=torch.float32).pin_memory()
+        bi = sum(v.numel() * v.element_size() for v in host.values())
+        bo = sum(v.numel() * v.element_size() for v in (h_tok, h_num, h_alpha))
+
+        def e2e_step():
+            for k in host:
+                dev_in[k].copy_(host[k], non_blocking=True)
+            sv.spec_verify(dev_in["target_logits"], dev_in["draft_logits"], dev_in["draft_tokens"],
+                           dev_in["draft_len"], dev_in["temperature"], dev_in["uniforms"],
+                           out_tokens, out_num, out_alpha, ws, stream)
+            h_tok.copy_(out_tokens, non_blocking=True)
+            h_num.copy_(out_num, non_blocking=True)
+            h_alpha.copy_(out_alpha, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ms_e2e = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            mt = torch.tensor([ms_e2e], device=dev)
+            torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(mt.item())
+        e2e = {"value": positions * world / (ms_e2e * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+               "ms_per_step": ms_e2e, "steps": n_e2e}
+        del host, dev_in
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        rate, rows, pos, secs = oracle_sample_rate(args.workload, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{rows} rows ({pos} positions) of the workload drawn on the host, "
+                         f"{secs:.1f} s of single-thread fp64 oracle work"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": cfg.name, "B": B, "gamma_max": G, "V": V, "logits": cfg.dtype,
+                       "greedy_rows": int((w.temperature == 0).sum()),
+                       "positions_per_gpu": positions, "padded_positions_per_gpu": B * (G + 1),
+                       "algorithmic_bytes_per_step": algo_bytes,
+                       "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                         "frac": achieved_gbs / peak, "peak_kind": peak_kind,
+                         "frac_of_8tbs": achieved_gbs / NORTH_STAR_HBM_GBS, "traffic": traffic,
+                         "kernel": "sv_stream_kernel<bf16>" if cfg.dtype == "bf16"
+                         else "sv_stream_kernel<f32>"},
+            "clocks": clock_info,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -70,8 +70,8 @@ typedef enum { SV_DTYPE_F32 = 0, SV_DTYPE_BF16 = 1 } sv_dtype;
 #define SV_MAX_GAMMA 64
 #define SV_VERSION 1
 
-/* Bytes of device workspace spec_verify needs for these sizes (per-position records and one arrival
- * counter per row), a multiple of 256. Returns 0 for invalid sizes.
+/* Bytes of device workspace spec_verify needs for these sizes (per-position records, one arrival
+ * counter per row and a status word), a multiple of 256. Returns 0 for invalid sizes.
  *
  * The workspace must hold zeros before its first use (e.g. one cudaMemset after allocation). Every
  * call that runs to completion leaves it zeroed again, so it can be reused without clearing. One
@@ -117,6 +117,14 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
                    float* out_p_draft, float* out_q_draft,
                    int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                    void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Reads the workspace's sticky status word into *status_out after synchronising `cuda_stream`
+ * (B and gamma_max as in the call that used the workspace). 0 means every call so far completed
+ * its protocol. A nonzero value means a kernel-internal wait gave up (every wait inside the
+ * kernels is bounded; on a healthy device none gives up): that call stopped early and the rows it
+ * had not finished keep stale outputs. The word stays set until the caller clears the workspace. */
+int spec_verify_workspace_status(const void* workspace, int32_t B, int32_t gamma_max,
+                                 int32_t* status_out, void* cuda_stream);
 
 /* Static description of an sv_status value (never NULL). */
 const char* spec_verify_status_string(int status);

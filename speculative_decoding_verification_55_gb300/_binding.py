@@ -23,7 +23,7 @@ STATUS_NAMES = {
 }
 
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
-            "spec_verify_status_string", "spec_verify_version")
+            "spec_verify_workspace_status", "spec_verify_status_string", "spec_verify_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -55,6 +55,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_ex.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
             L.spec_verify_workspace_size.restype = ctypes.c_size_t
+            L.spec_verify_workspace_status.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int32), vp]
+            L.spec_verify_workspace_status.restype = ctypes.c_int
             L.spec_verify_status_string.argtypes = [ctypes.c_int]
             L.spec_verify_status_string.restype = ctypes.c_char_p
             L.spec_verify_version.argtypes = []
@@ -69,6 +71,16 @@ def spec_verify_workspace_size(B: int, gamma_max: int, V: int, dtype: int) -> in
 
 def spec_verify_status_string(status: int) -> str:
     return lib().spec_verify_status_string(int(status)).decode()
+
+
+def spec_verify_workspace_status(workspace, B: int, gamma_max: int, stream=None) -> int:
+    """The workspace's sticky status word (0 = every call completed its protocol)."""
+    out = ctypes.c_int32(0)
+    st = lib().spec_verify_workspace_status(_ptr(workspace), B, gamma_max, ctypes.byref(out),
+                                            _stream_handle(stream, workspace.device))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_workspace_status")
+    return int(out.value)
 
 
 def spec_verify_version() -> int:

@@ -1,0 +1,226 @@
+// C ABI of the verifier (include/spec_verify.h): host-side validation, launch planning and
+// dispatch to the streaming kernel (16-byte aligned rows) or the element kernel (any alignment).
+
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/spec_verify.h"
+#include "sv_common.cuh"
+
+namespace {
+
+#ifndef SV_STREAM_CHUNK_BYTES
+#define SV_STREAM_CHUNK_BYTES 65536   // target bytes of one row chunk per CTA on the streaming path
+#endif
+#ifndef SV_STREAM_MAX_CLUSTER
+#define SV_STREAM_MAX_CLUSTER 8
+#endif
+
+constexpr int kElemThreads = 512;
+constexpr int kVptOptions[4] = {1, 2, 4, 8};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t records_bytes(int32_t B, int32_t G) {
+  return align_up(static_cast<size_t>(B) * (G + 1) * sizeof(int2), 256);
+}
+
+bool sizes_ok(int32_t B, int32_t G, int32_t V, int32_t dtype) {
+  if (B < 1 || G < 0 || G > SV_MAX_GAMMA || V < 1) return false;
+  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return false;
+  return true;
+}
+
+// Element path: a row of V logits split into C <= 16 chunks of at most 512 * VPT logits.
+bool element_plan(int V, int* vpt_index, int* C, int* per) {
+  for (int vi = 0; vi < 4; ++vi) {
+    const long long cap = static_cast<long long>(kElemThreads) * kVptOptions[vi];
+    const long long c = (V + cap - 1) / cap;
+    if (c <= sv::kMaxCluster) {
+      *vpt_index = vi;
+      *C = static_cast<int>(c < 1 ? 1 : c);
+      *per = (V + *C - 1) / *C;
+      return true;
+    }
+  }
+  return false;
+}
+
+// Streaming path: CTAs per position, the power of two that brings a row chunk near
+// SV_STREAM_CHUNK_BYTES (at most SV_STREAM_MAX_CLUSTER), raised until a chunk fits the per-vector
+// sums buffer. 0 when even 16 CTAs leave chunks too large.
+int stream_cluster_size(long long row_bytes) {
+  int C = 1;
+  while (C < SV_STREAM_MAX_CLUSTER && row_bytes > static_cast<long long>(C) * SV_STREAM_CHUNK_BYTES)
+    C *= 2;
+  const long long units = row_bytes / 16;
+  while ((units + C - 1) / C > sv::kStreamMaxUnits) {
+    if (C >= sv::kMaxCluster) return 0;
+    C *= 2;
+  }
+  return C;
+}
+
+std::mutex g_mu;
+int g_device_ok[64];                 // 0 unknown, 1 sm_103, 2 other
+int g_max_clusters[64][2][5];        // by device, bf16, log2(C); 0 = not queried
+
+int check_device(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SV_ERR_CUDA;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_device_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return SV_ERR_CUDA;
+    g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_device_ok[dev] == 1 ? SV_OK : SV_ERR_UNSUPPORTED_DEVICE;
+}
+
+int max_clusters(int dev, bool bf16, int C, int* n) {
+  int lg = 0;
+  while ((1 << lg) < C) ++lg;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int& slot = g_max_clusters[dev][bf16 ? 1 : 0][lg];
+  if (slot == 0) {
+    int m = 0;
+    if (sv::stream_max_clusters(bf16, C, &m) != cudaSuccess || m < 1) return SV_ERR_CUDA;
+    slot = m;
+  }
+  *n = slot;
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int32_t B, int32_t gamma_max, int32_t V, int32_t dtype) {
+  if (!sizes_ok(B, gamma_max, V, dtype)) return 0;
+  return align_up(records_bytes(B, gamma_max) + static_cast<size_t>(B) * sizeof(unsigned) + 4, 256);
+}
+
+const char* spec_verify_status_string(int status) {
+  switch (status) {
+    case SV_OK: return "SV_OK: success";
+    case SV_ERR_NULL_POINTER: return "SV_ERR_NULL_POINTER: a required pointer is NULL";
+    case SV_ERR_BAD_SHAPE: return "SV_ERR_BAD_SHAPE: B, gamma_max or V out of range";
+    case SV_ERR_BAD_DTYPE: return "SV_ERR_BAD_DTYPE: dtype is not SV_DTYPE_F32 or SV_DTYPE_BF16";
+    case SV_ERR_WORKSPACE_TOO_SMALL: return "SV_ERR_WORKSPACE_TOO_SMALL: workspace missing or too small";
+    case SV_ERR_MISALIGNED: return "SV_ERR_MISALIGNED: a pointer is not aligned to its element type";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA runtime call failed";
+    case SV_ERR_UNSUPPORTED_DEVICE: return "SV_ERR_UNSUPPORTED_DEVICE: the device is not sm_103";
+    default: return "unknown sv_status";
+  }
+}
+
+int spec_verify_version(void) { return SV_VERSION; }
+
+int spec_verify_workspace_status(const void* workspace, int32_t B, int32_t gamma_max,
+                                 int32_t* status_out, void* cuda_stream) {
+  if (!workspace || !status_out) return SV_ERR_NULL_POINTER;
+  if (B < 1 || gamma_max < 0 || gamma_max > SV_MAX_GAMMA) return SV_ERR_BAD_SHAPE;
+  const char* w = static_cast<const char*>(workspace) + records_bytes(B, gamma_max) +
+                  static_cast<size_t>(B) * sizeof(unsigned);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, w, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SV_ERR_CUDA;
+  *status_out = static_cast<int32_t>(v);
+  return SV_OK;
+}
+
+int spec_verify_ex(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                   const int32_t* draft_len, const float* temperature, const float* uniforms,
+                   int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                   float* out_p_draft, float* out_q_draft,
+                   int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                   void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
+  if (!sizes_ok(B, gamma_max, V, dtype)) return SV_ERR_BAD_SHAPE;
+  const int G = gamma_max;
+  if (!target_logits || !temperature || !uniforms || !out_tokens || !out_num_emitted)
+    return SV_ERR_NULL_POINTER;
+  if (G > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_NULL_POINTER;
+  const bool bf16 = dtype == SV_DTYPE_BF16;
+  const uintptr_t es = bf16 ? 2 : 4;
+  auto mis = [](const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; };
+  if (mis(target_logits, es) || mis(draft_logits, es) || mis(draft_tokens, 4) || mis(draft_len, 4) ||
+      mis(temperature, 4) || mis(uniforms, 4) || mis(out_tokens, 4) || mis(out_num_emitted, 4) ||
+      mis(out_alpha, 4) || mis(out_p_draft, 4) || mis(out_q_draft, 4) || mis(workspace, 16))
+    return SV_ERR_MISALIGNED;
+  const size_t need = spec_verify_workspace_size(B, G, V, dtype);
+  if (!workspace || workspace_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
+  if (static_cast<long long>(B) * (G + 1) > INT_MAX / sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
+
+  const bool vec = (static_cast<size_t>(V) * es) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
+                   (!draft_logits || reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0);
+  int vpt_index = 0, eC = 1, eper = 1;
+  if (!vec && !element_plan(V, &vpt_index, &eC, &eper)) return SV_ERR_BAD_SHAPE;
+  const int sC = vec ? stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es)) : 0;
+  if (vec && sC == 0) return SV_ERR_BAD_SHAPE;
+
+  int dev = 0;
+  const int dev_status = check_device(&dev);
+  if (dev_status != SV_OK) return dev_status;
+
+  sv::Params P;
+  P.zt = target_logits;
+  P.zd = draft_logits;
+  P.tokens = draft_tokens;
+  P.draft_len = draft_len;
+  P.temperature = temperature;
+  P.uniforms = uniforms;
+  P.out_tokens = out_tokens;
+  P.out_num = out_num_emitted;
+  P.out_alpha = out_alpha;
+  P.out_p = out_p_draft;
+  P.out_q = out_q_draft;
+  char* ws = static_cast<char*>(workspace);
+  P.rec = reinterpret_cast<int2*>(ws);
+  P.cnt = reinterpret_cast<unsigned*>(ws + records_bytes(B, G));
+  P.status = P.cnt + B;
+  P.B = B;
+  P.G = G;
+  P.V = V;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+
+  if (vec) {
+    const int E = static_cast<int>(16 / es);
+    P.units = V / E;
+    P.C = sC;
+    P.per = (P.units + P.C - 1) / P.C;
+    int maxc = 0;
+    if (max_clusters(dev, bf16, P.C, &maxc) != SV_OK) return SV_ERR_CUDA;
+    const long long slots = static_cast<long long>(B) * (G + 1);
+    P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
+    if (sv::launch_stream(P, bf16, stream) != cudaSuccess) return SV_ERR_CUDA;
+    return SV_OK;
+  }
+  P.units = V;
+  P.C = eC;
+  P.per = eper;
+  P.nclusters = B * (G + 1);
+  if (sv::launch_element(P, bf16, vpt_index, stream) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                const int32_t* draft_len, const float* temperature, const float* uniforms,
+                int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                        out_tokens, out_num_emitted, out_alpha, nullptr, nullptr, B, gamma_max, V,
+                        dtype, workspace, workspace_bytes, cuda_stream);
+}
+
+}  // extern "C"

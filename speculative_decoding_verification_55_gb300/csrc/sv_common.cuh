@@ -1,0 +1,430 @@
+// Shared device code of the sm_103a verification kernels: kernel parameters, inline-PTX helpers
+// (exp2, NaN-propagating max, clusters, mbarriers, bulk copies), warp reductions, and the
+// per-position finish (record, arrival counter, row emit) both kernels end with.
+//
+// The operation is defined on these pages (page title, section):
+//   [R] "Speculative decoding", rayaq.ca ml-models -- Mechanics, One round, steps 3-5; Why the
+//       output is exactly the target's; The greedy case; Implementation.
+//   [B] "Inference: distillation and speculative decoding", brunomaga.github.io -- Draft-model
+//       speculative decoding (greedy rule, speculative-sampling rule, ragged batched rows).
+//   [C] "Speculative decoding", cgnarendiran.github.io blog -- The correction that makes it exact.
+// p is the target distribution, q the draft distribution.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+
+namespace sv {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxCluster = 16;
+// Largest chunk (in 16-byte vectors) one CTA of the streaming kernel owns per row: its per-vector
+// residual sums must fit in shared memory beside the copy ring.
+constexpr int kStreamMaxUnits = 4864;
+
+enum : int { kVerify = 0, kBonus = 1, kArgmax = 2 };
+enum : int { kFlagAccept = 1, kFlagBad = 2 };
+
+struct Params {
+  const void* zt;            // [B, G+1, V] target logits
+  const void* zd;            // [B, G, V] draft logits
+  const int32_t* tokens;     // [B, G] drafted tokens
+  const int32_t* draft_len;  // [B] or null
+  const float* temperature;  // [B]
+  const float* uniforms;     // [B, G+2]
+  int32_t* out_tokens;       // [B, G+1]
+  int32_t* out_num;          // [B]
+  float* out_alpha;          // [B, G] or null
+  float* out_p;              // [B, G] or null
+  float* out_q;              // [B, G] or null
+  int2* rec;                 // [B, G+1] per-position records {candidate token, flags}
+  unsigned* cnt;             // [B] arrival counters (zero between calls)
+  unsigned* status;          // [1] sticky kernel status (0 = fine)
+  int B, G, V;
+  int C;                     // CTAs per position (cluster size)
+  int units;                 // load units per row (16-byte vectors, or logits on the element path)
+  int per;                   // units per CTA chunk
+  int nclusters;             // clusters in the grid (persistent kernel)
+};
+
+// ------------------------------------------------------------------------------------------------
+// Arithmetic
+// ------------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Packed fp32 pairs (sm_100+ f32x2 arithmetic).
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(f32x2 v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Memory
+// ------------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// One stored logit widened to fp32 (exact for both storage types).
+template <bool BF16>
+__device__ __forceinline__ float load_logit(const void* row, int v) {
+  if (BF16) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + v);
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  return __ldg(reinterpret_cast<const float*>(row) + v);
+}
+
+// Logit e (0 <= e < 8 for bf16, < 4 for fp32) of a 16-byte vector.
+template <bool BF16>
+__device__ __forceinline__ float vec_get(const uint4& v, int e) {
+  const int w = BF16 ? (e >> 1) : e;
+  const uint32_t x = w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+  if (BF16) return __uint_as_float((e & 1) ? (x & 0xffff0000u) : (x << 16));
+  return __uint_as_float(x);
+}
+
+// NaN-propagating max of the logits of a 16-byte vector.
+template <bool BF16>
+__device__ __forceinline__ float vec_max(const uint4& v) {
+  if (BF16) {
+    const uint32_t m = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
+    return max_nan(bf_lo(m), bf_hi(m));
+  }
+  return max_nan(max_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                 max_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+
+// ------------------------------------------------------------------------------------------------
+// Clusters and mbarriers
+// ------------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v4f32(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
+               ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init_cluster() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded waits: every spin gives up after kSpinLimit polls (each poll may suspend the thread for a
+// hardware-chosen time), so a broken protocol ends the kernel with an error status instead of a hang.
+constexpr int kSpinLimit = 1 << 22;
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int n = 0; n < kSpinLimit; ++n)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
+  for (int n = 0; n < kSpinLimit; ++n)
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+  return false;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// Arrive on an mbarrier of any CTA of the cluster, releasing this thread's earlier writes.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Bulk copy global -> this CTA's shared memory, completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
+// Warp reductions
+// ------------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum_lane0(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return __shfl_sync(kFull, v, 0);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+// (value, index) argmax over the warp: larger value wins, equal values keep the lower index.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(kFull, v, o);
+    const int oi = __shfl_xor_sync(kFull, i, o);
+    if (ov > v || (ov == v && oi < i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Row scalars and row errors
+// ------------------------------------------------------------------------------------------------
+
+// Writes the all-error outputs of row b (one full warp).
+__device__ __forceinline__ void write_row_error(const Params& P, int b, int lane) {
+  const int G = P.G;
+  for (int j = lane; j <= G; j += 32) P.out_tokens[(size_t)b * (G + 1) + j] = -1;
+  for (int j = lane; j < G; j += 32) {
+    if (P.out_alpha) P.out_alpha[(size_t)b * G + j] = 0.0f;
+    if (P.out_p) P.out_p[(size_t)b * G + j] = 0.0f;
+    if (P.out_q) P.out_q[(size_t)b * G + j] = 0.0f;
+  }
+  if (lane == 0) P.out_num[b] = -1;
+}
+
+// Drafted tokens in [0, V) for i < gamma_b, and (sampled rows) the used uniforms in [0, 1). Every
+// lane of the warp returns the same answer.
+__device__ __forceinline__ bool row_scalars_ok(const Params& P, int b, int gb, bool greedy, int lane) {
+  const int G = P.G;
+  bool good = true;
+  const int32_t* xr = P.tokens + (size_t)b * G;
+  for (int j = lane; j < gb; j += 32) {
+    const int x = __ldg(xr + j);
+    good &= (x >= 0 && x < P.V);
+  }
+  if (!greedy) {
+    const float* ur = P.uniforms + (size_t)b * (G + 2);
+    for (int j = lane; j < gb + 2; j += 32) {
+      const float u = __ldg(ur + (j < gb ? j : G + (j - gb)));
+      good &= (u >= 0.0f && u < 1.0f);
+    }
+  }
+  return __all_sync(kFull, good);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Finish a position (one full warp of the CTA that holds the position's final result): outputs of
+// the position, its record, its arrival on the row counter and, for the row's last arrival, the
+// row's emit: k = first rejected position (else gamma_b), tokens x_0..x_{k-1} then the correction
+// or bonus token ([R] One round, steps 3-5). The counter scheme needs no waiting: the arrivals are
+// ordered by release fences and the last one acquires.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void finish_position(const Params& P, int b, int i, int gb, int cand,
+                                                int flags, float alpha, float px, float qx,
+                                                int lane) {
+  const int G = P.G, G1 = G + 1;
+  if (lane == 0 && i < gb) {
+    if (P.out_alpha) P.out_alpha[(size_t)b * G + i] = alpha;
+    if (P.out_p) P.out_p[(size_t)b * G + i] = px;
+    if (P.out_q) P.out_q[(size_t)b * G + i] = qx;
+  }
+  if (i == gb) {
+    for (int j = gb + lane; j < G; j += 32) {   // padding positions of the row
+      if (P.out_alpha) P.out_alpha[(size_t)b * G + j] = 0.0f;
+      if (P.out_p) P.out_p[(size_t)b * G + j] = 0.0f;
+      if (P.out_q) P.out_q[(size_t)b * G + j] = 0.0f;
+    }
+  }
+  unsigned old = 0;
+  __syncwarp();
+  if (lane == 0) {
+    P.rec[(size_t)b * G1 + i] = make_int2(cand, flags);
+    __threadfence();
+    old = atomicAdd(P.cnt + b, 1u);
+  }
+  old = __shfl_sync(kFull, old, 0);
+  if (old != static_cast<unsigned>(gb)) return;
+  __threadfence();
+
+  int kk = gb;
+  bool err = false;
+  for (int j0 = 0; j0 <= gb; j0 += 32) {
+    const int j = j0 + lane;
+    int2 r = make_int2(-1, kFlagAccept);
+    if (j <= gb) r = __ldcg(P.rec + (size_t)b * G1 + j);
+    err |= (j <= gb) && (r.y & kFlagBad);
+    const unsigned rej = __ballot_sync(kFull, j < gb && !(r.y & kFlagAccept));
+    if (rej && kk == gb) kk = j0 + __ffs(rej) - 1;
+  }
+  err = __any_sync(kFull, err);
+  const int tok_k = __ldcg(P.rec + (size_t)b * G1 + kk).x;
+  err = err || tok_k < 0;
+  __syncwarp();
+  for (int j = lane; j <= gb; j += 32) P.rec[(size_t)b * G1 + j] = make_int2(0, 0);  // leave zeros
+  for (int j = lane; j <= G; j += 32) {
+    int v = -1;
+    if (!err) v = (j < kk) ? __ldg(P.tokens + (size_t)b * G + j) : (j == kk ? tok_k : -1);
+    P.out_tokens[(size_t)b * G1 + j] = v;
+  }
+  if (err) {
+    for (int j = lane; j < G; j += 32) {
+      if (P.out_alpha) P.out_alpha[(size_t)b * G + j] = 0.0f;
+      if (P.out_p) P.out_p[(size_t)b * G + j] = 0.0f;
+      if (P.out_q) P.out_q[(size_t)b * G + j] = 0.0f;
+    }
+  }
+  if (lane == 0) {
+    P.out_num[b] = err ? -1 : kk + 1;
+    P.cnt[b] = 0u;                                     // leave the workspace zeroed
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Host-side launchers (defined in the kernel translation units)
+// ------------------------------------------------------------------------------------------------
+
+// Element path (any alignment, V <= 16 * 512 * 8): one cluster per position slot.
+cudaError_t launch_element(const Params& P, bool bf16, int vpt_index, cudaStream_t stream);
+// Streaming path (16-byte aligned rows): persistent clusters fed by bulk copies.
+cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream);
+// Clusters of `C` CTAs of the streaming kernel that fit on the current device at once.
+cudaError_t stream_max_clusters(bool bf16, int C, int* n);
+
+}  // namespace sv

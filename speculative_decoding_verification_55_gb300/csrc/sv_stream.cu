@@ -1,0 +1,746 @@
+// Streaming path of the sm_103a verifier (rows of 16-byte multiples): persistent thread-block
+// clusters fed by bulk copies.
+//
+// Work split. A position (b, i) of the batch is one target row (plus the draft row for a drafted
+// position) of V logits. Each cluster of C CTAs owns every nclusters-th position slot; CTA r of the
+// cluster owns the r-th contiguous chunk of every row it touches. Two CTAs share an SM, so one
+// CTA's exchanges and barriers overlap the other's arithmetic. A CTA is 8 consumer warps and one
+// producer warp.
+//
+// Producer warp (one thread). Walks the cluster's positions and streams this CTA's chunks through a
+// ring of kNumSlots x 16 KB shared-memory slots with cp.async.bulk (the TMA engine), one full/empty
+// mbarrier pair per slot. It runs ahead of the consumers by the ring's capacity, so HBM keeps
+// streaming while the consumers exchange partial results.
+//
+// Consumer warps, per position:
+//   pass 1   online softmax of the chunk straight out of the ring: running max (with a
+//            NaN-propagating tracker beside it) and sum of exp2((z - m) log2(e) / T); greedy rows:
+//            running argmax with the lowest index.
+//   xchg 1   CTA partials are pushed into every CTA of the cluster (st.shared::cluster) with a remote
+//            mbarrier arrival; each CTA combines the C records in the same fixed order: global max
+//            M, normaliser S (an inclusive scan over ranks = the chunk-level CDF of p), the accept
+//            test u < min(1, p(x)/q(x)), the chunk that holds a bonus-draw threshold.
+//   pass 2   (drafted positions) the chunk again, now from L2 where pass 1 left it: residual
+//            weights max(0, p - q), p and q normalised inside the exponent; one sum per 16-byte
+//            vector is kept in shared memory for the draw. alpha = 1 - W with W the residual mass:
+//            sum min(p, q) + sum max(0, p - q) = sum p = 1 ([R] Why the output is exactly the
+//            target's).
+//   xchg 2   residual chunk totals (inclusive scan over ranks).
+//   draw     the CTA whose chunk holds the inverse-CDF threshold scans its per-vector sums in index
+//            order (block-wide prefix sum), reloads the one vector that crosses the threshold and
+//            picks the token inside it. A bonus draw first fills the per-vector sums of p from L2.
+//   finish   the CTA holding the position's final result writes it; the row's last position to
+//            finish writes the row's outputs (an arrival counter per row, no waiting).
+// Every wait is bounded; a wait that gives up sets the status word and ends the kernel.
+//
+// The operation: [R] "Speculative decoding", rayaq.ca ml-models -- Mechanics, One round, steps 3-5;
+// Why the output is exactly the target's; The greedy case; Implementation. [B]
+// brunomaga.github.io "Inference: distillation and speculative decoding" -- Draft-model speculative
+// decoding. [C] cgnarendiran.github.io "Speculative decoding" -- The correction that makes it exact.
+
+#include "sv_common.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kCW = 8;                        // consumer warps
+constexpr int kCT = kCW * 32;                 // consumer threads
+constexpr int kThreadsS = kCT + 32;           // plus the producer warp
+constexpr int kSlotBytes = 16384;
+constexpr int kSlotUnits = kSlotBytes / 16;
+constexpr int kNumSlots = 5;
+constexpr int kRingBytes = kSlotBytes * kNumSlots;
+constexpr int kDynBytes = kRingBytes + kStreamMaxUnits * 4;   // ring + per-vector sums
+constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
+
+enum : unsigned { kStatusTimeout = 1u };
+
+struct Shared {
+  uint64_t full[kNumSlots];
+  uint64_t empty[kNumSlots];
+  uint64_t xbar1[2];                 // exchange 1 arrivals (one per CTA), by exchange parity
+  uint64_t xbar2[2];                 // exchange 2 arrivals
+  uint64_t xdone;                    // end-of-kernel arrivals
+  float4 xch1[2][kMaxCluster];       // records pushed by every rank, exchange 1
+  int xbad1[2][kMaxCluster];
+  float xch2[2][kMaxCluster];        // residual chunk totals, exchange 2
+  float4 wpart[kCW];                 // warp partials
+  int wbad[kCW];
+  int widx[kCW];
+  float wsum2[kCW];
+  float scan_wt[kCW];
+  int scan_slot[kCW];
+  int stop;                          // set by any thread that gave up a wait
+  int stop_snap;                     // its value as published by consumer warp 0 under a barrier
+  // per-position broadcast from consumer warp 0
+  float k, ct, cd, cb;               // log2(e)/T; exponent offsets of p, q and of unnormalised p
+  float px, qx, alpha, t_local;
+  int acc, bad, cand, draw_chunk, draw_resid;
+  int p_chunk;                       // chunk of a draw from p with the residual uniform
+  float p_tlocal;
+};
+
+struct Pos {
+  int b, i, gb;
+  float T;
+  bool len_ok, t_ok, greedy, load, two;
+};
+
+__device__ __forceinline__ Pos classify(const Params& P, int s) {
+  Pos p;
+  const int G1 = P.G + 1;
+  p.b = s / G1;
+  p.i = s - p.b * G1;
+  p.gb = P.draft_len ? __ldg(P.draft_len + p.b) : P.G;
+  p.T = __ldg(P.temperature + p.b);
+  p.len_ok = p.gb >= 0 && p.gb <= P.G;
+  p.greedy = (p.T == 0.0f);
+  p.t_ok = p.greedy || (p.T >= FLT_MIN && p.T <= FLT_MAX);   // NaN fails both
+  p.load = p.len_ok && p.t_ok && p.i <= p.gb;
+  p.two = p.load && !p.greedy && p.i < p.gb;
+  return p;
+}
+
+__device__ __forceinline__ void set_status(const Params& P, Shared& sm, unsigned code) {
+  atomicOr(P.status, code);
+  sm.stop = 1;
+}
+
+// Pass-1 update of a running (max m, sum s) with the 8 or 4 logits of one vector.
+template <bool BF16>
+__device__ __forceinline__ void online_update(const uint4& v, float k, float& m, f32x2& s, float& mx) {
+  const float vm = vec_max<BF16>(v);
+  mx = max_nan(mx, vm);
+  if (vm > m) {                                   // rescale the running sum to the new max
+    float s0, s1;
+    upk(s, s0, s1);
+    const float f = ex2((m - vm) * k);
+    s = pk(s0 * f, s1 * f);
+    m = vm;
+  }
+  const float c = -m * k;
+  const f32x2 k2 = pk(k, k), c2 = pk(c, c);
+  if (BF16) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float a0, a1;
+      upk(fma2(pk(bf_lo(w[j]), bf_hi(w[j])), k2, c2), a0, a1);
+      s = add2(s, pk(ex2(a0), ex2(a1)));
+    }
+  } else {
+    float a0, a1, a2, a3;
+    upk(fma2(pk(__uint_as_float(v.x), __uint_as_float(v.y)), k2, c2), a0, a1);
+    upk(fma2(pk(__uint_as_float(v.z), __uint_as_float(v.w)), k2, c2), a2, a3);
+    s = add2(s, pk(ex2(a0), ex2(a1)));
+    s = add2(s, pk(ex2(a2), ex2(a3)));
+  }
+}
+
+// Pass-1 greedy update: running max and the lowest index holding it.
+template <bool BF16>
+__device__ __forceinline__ void argmax_update(const uint4& v, int base, float& m, int& idx, float& mx) {
+  constexpr int E = BF16 ? 8 : 4;
+  const float vm = vec_max<BF16>(v);
+  mx = max_nan(mx, vm);
+  if (vm > m) {
+#pragma unroll
+    for (int e = E - 1; e >= 0; --e)
+      if (vec_get<BF16>(v, e) == vm) idx = base + e;
+    m = vm;
+  }
+}
+
+// Residual weights max(0, p - q) of element pair e, e+1 of a target vector and its draft vector,
+// p and q normalised inside the exponent (ct, cd), two logits per packed instruction.
+template <bool BF16>
+__device__ __forceinline__ void resid_pair(const uint4& t, const uint4& d, int e, f32x2 k2, f32x2 c2,
+                                           float& w0, float& w1) {
+  float a0, b0, a1, b1;
+  upk(fma2(pk(vec_get<BF16>(t, e), vec_get<BF16>(d, e)), k2, c2), a0, b0);
+  upk(fma2(pk(vec_get<BF16>(t, e + 1), vec_get<BF16>(d, e + 1)), k2, c2), a1, b1);
+  upk(sub2(pk(ex2(a0), ex2(a1)), pk(ex2(b0), ex2(b1))), w0, w1);
+  w0 = fmaxf(w0, 0.0f);
+  w1 = fmaxf(w1, 0.0f);
+}
+
+// Sum of the residual weights of one vector pair (the order the draw's rescan reproduces).
+template <bool BF16>
+__device__ __forceinline__ float resid_vec_sum(const uint4& t, const uint4& d, f32x2 k2, f32x2 c2) {
+  constexpr int E = BF16 ? 8 : 4;
+  float s = 0.0f;
+#pragma unroll
+  for (int e = 0; e < E; e += 2) {
+    float w0, w1;
+    resid_pair<BF16>(t, d, e, k2, c2, w0, w1);
+    s += w0;
+    s += w1;
+  }
+  return s;
+}
+
+// Sum of the unnormalised p weights exp2(z k + cb) of one vector.
+template <bool BF16>
+__device__ __forceinline__ float p_vec_sum(const uint4& t, float k, float cb) {
+  constexpr int E = BF16 ? 8 : 4;
+  float s = 0.0f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) s += ex2(fmaf(vec_get<BF16>(t, e), k, cb));
+  return s;
+}
+
+// The draw inside this CTA's chunk. usum[j] holds the weight of vector u0 + j (residual or p
+// weights, per `resid`); the token is the first logit whose running weight exceeds t_local, else
+// (rounding) the last logit with positive weight. Block-wide prefix sum over the vector sums, then
+// one reload of the crossing vector. Returns the token in warp `finisher` (all its lanes); other
+// warps return -1. All consumer threads call it.
+template <bool BF16>
+__device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, const char* rowt,
+                          const char* rowd, bool resid, float k, float ct, float cd, float cb,
+                          Shared& sm, int ctid, int& finisher) {
+  constexpr int E = BF16 ? 8 : 4;
+  const int lane = ctid & 31, cw = ctid >> 5;
+  const int run = (cu + kCT - 1) / kCT;
+  const int r0 = min(ctid * run, cu), r1 = min(r0 + run, cu);
+  float tsum = 0.0f;
+  int last_j = -1;
+  for (int j = r0; j < r1; ++j) {
+    const float v = usum[j];
+    tsum += v;
+    if (v > 0.0f) last_j = j;
+  }
+  const float incl = warp_incl_scan(tsum, lane);
+  float excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.0f;
+  if (lane == 31) sm.scan_wt[cw] = incl;
+  int lj = last_j;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lj = max(lj, __shfl_xor_sync(kFull, lj, o));
+  if (lane == 0) sm.widx[cw] = lj;
+  named_bar_sync(kConsumerBar, kCT);
+  float wexcl = 0.0f;
+#pragma unroll
+  for (int w2 = 0; w2 < kCW; ++w2)
+    if (w2 < cw) wexcl += sm.scan_wt[w2];
+  const bool cross = (tsum > 0.0f) && (wexcl + incl > t_local);
+  const unsigned m = __ballot_sync(kFull, cross);
+  if (lane == 0) sm.scan_slot[cw] = m ? (cw * 32 + __ffs(m) - 1) : INT_MAX;
+  named_bar_sync(kConsumerBar, kCT);
+  int win = INT_MAX, best_j = -1;
+#pragma unroll
+  for (int w2 = 0; w2 < kCW; ++w2) {
+    win = min(win, sm.scan_slot[w2]);
+    best_j = max(best_j, sm.widx[w2]);
+  }
+  // The crossing vector and the weight before it (winner thread), else the last positive vector.
+  finisher = (win == INT_MAX) ? 0 : (win >> 5);
+  if (cw != finisher) return -1;
+  int vj = -1;
+  float before = 0.0f;
+  bool overrun = (win == INT_MAX);
+  if (!overrun && ctid == win) {
+    float c = wexcl + excl;
+    int lastpos = -1;
+    float c_last = c;
+    for (int j = r0; j < r1; ++j) {
+      const float v = usum[j];
+      if (v > 0.0f) {
+        if (c + v > t_local) {
+          vj = j;
+          before = c;
+          break;
+        }
+        lastpos = j;
+        c_last = c;
+        c += v;
+      }
+    }
+    if (vj < 0) {          // rounding: the run's sums crossed, its vectors did not
+      vj = lastpos;
+      before = c_last;
+      overrun = true;
+    }
+  }
+  const int src = overrun && win == INT_MAX ? 0 : (win & 31);
+  vj = overrun && win == INT_MAX ? best_j : __shfl_sync(kFull, vj, src);
+  before = __shfl_sync(kFull, before, src);
+  overrun = __shfl_sync(kFull, overrun ? 1 : 0, src) != 0;
+  int tok = -1;
+  if (lane == 0 && vj >= 0) {
+    const int u = u0 + vj;
+    const uint4 t = ld_stream_v4(reinterpret_cast<const uint4*>(rowt) + u);
+    const uint4 d = resid ? ld_stream_v4(reinterpret_cast<const uint4*>(rowd) + u) : t;
+    const f32x2 k2 = pk(k, k), c2 = pk(ct, cd);
+    float c = before;
+    int pick = -1, lastp = -1;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      float w0, w1;
+      if (resid) {
+        resid_pair<BF16>(t, d, e, k2, c2, w0, w1);
+      } else {
+        w0 = ex2(fmaf(vec_get<BF16>(t, e), k, cb));
+        w1 = ex2(fmaf(vec_get<BF16>(t, e + 1), k, cb));
+      }
+      if (w0 > 0.0f) {
+        lastp = e;
+        c += w0;
+        if (pick < 0 && c > t_local) pick = e;
+      }
+      if (w1 > 0.0f) {
+        lastp = e + 1;
+        c += w1;
+        if (pick < 0 && c > t_local) pick = e + 1;
+      }
+    }
+    if (pick < 0 || overrun) pick = lastp;
+    tok = pick >= 0 ? u * E + pick : -1;
+  }
+  return __shfl_sync(kFull, tok, 0);
+}
+
+// Lane r < C of the calling warp pushes a record into CTA r's slot `slot_addr` (same offset in every
+// CTA) and arrives on CTA r's barrier.
+__device__ __forceinline__ void push_record4(uint32_t slot_addr, uint32_t bad_addr, uint32_t bar,
+                                             float4 v, int bad, int C, int lane) {
+  if (lane < C) {
+    st_cluster_v4f32(map_to_rank(slot_addr, lane), v.x, v.y, v.z, v.w);
+    st_cluster_s32(map_to_rank(bad_addr, lane), bad);
+    mbar_arrive_remote(map_to_rank(bar, lane));
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ Shared sm;
+  constexpr size_t ES = BF16 ? 2 : 4;
+  constexpr int E = BF16 ? 8 : 4;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = static_cast<int>(cluster_rank());
+  const int C = P.C, G = P.G, G1 = G + 1;
+  const int cid = static_cast<int>(blockIdx.x) / C;
+  const int total = P.B * G1;
+  const int u0 = min(rank * P.per, P.units);
+  const int u1 = min(u0 + P.per, P.units);
+  const int cu = u1 - u0;
+  const int nsl = (cu + kSlotUnits - 1) / kSlotUnits;
+  const size_t Vs = static_cast<size_t>(P.V);
+  float* usum = reinterpret_cast<float*>(dyn + kRingBytes);
+
+  if (tid == 0) {
+    for (int s = 0; s < kNumSlots; ++s) {
+      mbar_init(smem_addr(&sm.full[s]), 1);
+      mbar_init(smem_addr(&sm.empty[s]), kCW);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&sm.xbar1[s]), C);
+      mbar_init(smem_addr(&sm.xbar2[s]), C);
+    }
+    mbar_init(smem_addr(&sm.xdone), C);
+    sm.stop = 0;
+    sm.stop_snap = 0;
+    fence_mbarrier_init_cluster();
+  }
+  cluster_sync_all();                      // every CTA's barriers exist before any remote arrival
+
+  const uint32_t ring_addr = smem_addr(dyn);
+
+  // ------------------------------------------------------------------ producer
+  if (warp == kCW) {
+    if (lane != 0) return;
+    uint32_t tc = 0;
+    bool ok = true;
+    for (int s = cid; s < total && ok; s += P.nclusters) {
+      const Pos p = classify(P, s);
+      if (!p.load) continue;
+      for (int row = 0; row < (p.two ? 2 : 1) && ok; ++row) {
+        const char* g = row == 0
+            ? static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES
+            : static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES;
+        g += static_cast<size_t>(u0) * 16;
+        for (int ks = 0; ks < nsl; ++ks, ++tc) {
+          const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
+          if (!mbar_wait(smem_addr(&sm.empty[slot]), par ^ 1) || sm.stop) {
+            ok = false;
+            break;
+          }
+          const uint32_t bytes = static_cast<uint32_t>(min(kSlotUnits, cu - ks * kSlotUnits)) * 16;
+          mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), bytes);
+          bulk_g2s(ring_addr + slot * kSlotBytes, g + static_cast<size_t>(ks) * kSlotBytes, bytes,
+                   smem_addr(&sm.full[slot]));
+        }
+      }
+    }
+    if (!ok) {
+      set_status(P, sm, kStatusTimeout);
+      // Let the copies already issued land before this CTA can exit.
+      for (uint32_t t = tc > kNumSlots ? tc - kNumSlots : 0; t < tc; ++t)
+        mbar_wait(smem_addr(&sm.full[t % kNumSlots]), (t / kNumSlots) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  const int ctid = tid;          // 0 .. kCT-1
+  const int cw = warp;
+  uint32_t tc = 0;               // ring slots consumed
+  uint32_t e1 = 0, e2 = 0;       // exchanges done
+  const uint4* ringv = reinterpret_cast<const uint4*>(dyn);
+
+  for (int s = cid; s < total; s += P.nclusters) {
+    const Pos p = classify(P, s);
+    if (!p.load) {
+      if (!(p.len_ok && p.t_ok) && p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
+      continue;
+    }
+    const bool ok = row_scalars_ok(P, p.b, p.gb, p.greedy, lane);
+    const int kind = p.greedy ? kArgmax : (p.two ? kVerify : kBonus);
+    const char* rowt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES;
+    const char* rowd = p.two ? static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES
+                             : nullptr;
+    const int x = p.i < p.gb ? __ldg(P.tokens + (size_t)p.b * G + p.i) : -1;
+
+    // Early scalar loads for the accept test (their latency hides behind pass 1).
+    float zx_t = 0.0f, zx_d = 0.0f, u_acc = 0.0f, u_res = 0.0f, u_bon = 0.0f;
+    if (ok && cw == 0 && !p.greedy) {
+      const float* ur = P.uniforms + (size_t)p.b * (G + 2);
+      u_res = __ldg(ur + G);
+      u_bon = __ldg(ur + G + 1);
+      if (kind == kVerify) {
+        u_acc = __ldg(ur + p.i);
+        zx_t = load_logit<BF16>(rowt, x);
+        zx_d = load_logit<BF16>(rowd, x);
+      }
+    }
+
+    // ---- pass 1 out of the ring ----
+    const float k = p.greedy ? 0.0f : kLog2e / p.T;
+    float mt = -INFINITY, md = -INFINITY, mxt = -INFINITY, mxd = -INFINITY;
+    f32x2 st = pk(0.0f, 0.0f), sd = pk(0.0f, 0.0f);
+    int idx = INT_MAX;
+    bool timed_out = false;
+    for (int row = 0; row < (p.two ? 2 : 1); ++row) {
+      for (int ks = 0; ks < nsl; ++ks, ++tc) {
+        const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
+        if (!mbar_wait(smem_addr(&sm.full[slot]), par)) timed_out = true;
+        const int nu = min(kSlotUnits, cu - ks * kSlotUnits);
+        const uint4* src = ringv + slot * kSlotUnits;
+        if (ok && !timed_out) {
+          if (kind == kArgmax) {
+            for (int uu = ctid; uu < nu; uu += kCT)
+              argmax_update<BF16>(src[uu], (u0 + ks * kSlotUnits + uu) * E, mt, idx, mxt);
+          } else if (row == 0) {
+            for (int uu = ctid; uu < nu; uu += kCT) online_update<BF16>(src[uu], k, mt, st, mxt);
+          } else {
+            for (int uu = ctid; uu < nu; uu += kCT) online_update<BF16>(src[uu], k, md, sd, mxd);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+      }
+    }
+    if (timed_out) set_status(P, sm, kStatusTimeout);
+    if (!ok) {                       // drafted token or uniform out of range: the row is an error
+      if (p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
+      continue;
+    }
+
+    // ---- warp partials ----
+    if (kind == kArgmax) {
+      warp_argmax(mt, idx);
+      const int bad = __any_sync(kFull, (mxt != mxt) || mxt == INFINITY);
+      if (lane == 0) {
+        sm.wpart[cw] = make_float4(mt, 0.0f, 0.0f, 0.0f);
+        sm.widx[cw] = idx;
+        sm.wbad[cw] = bad;
+      }
+    } else {
+      float s0, s1;
+      upk(st, s0, s1);
+      float sT = s0 + s1;
+      upk(sd, s0, s1);
+      float sD = s0 + s1;
+      const float Mwt = warp_max(mt), Mwd = warp_max(md);
+      sT = (sT > 0.0f) ? sT * ex2((mt - Mwt) * k) : 0.0f;
+      sD = (sD > 0.0f) ? sD * ex2((md - Mwd) * k) : 0.0f;
+      sT = warp_sum_lane0(sT);
+      sD = warp_sum_lane0(sD);
+      const float mxa = max_nan(mxt, mxd);
+      const int bad = __any_sync(kFull, (mxa != mxa) || mxa == INFINITY);
+      if (lane == 0) {
+        sm.wpart[cw] = make_float4(Mwt, sT, Mwd, sD);
+        sm.wbad[cw] = bad;
+      }
+    }
+    named_bar_sync(kConsumerBar, kCT);
+
+    // ---- exchange 1 (consumer warp 0) ----
+    const uint32_t par1 = e1 & 1, ph1 = (e1 >> 1) & 1;
+    ++e1;
+    if (cw == 0) {
+      float4 rec;
+      if (kind == kArgmax) {
+        float v = lane < kCW ? sm.wpart[lane].x : -INFINITY;
+        int ii = lane < kCW ? sm.widx[lane] : INT_MAX;
+        warp_argmax(v, ii);
+        rec = make_float4(v, __int_as_float(ii), 0.0f, 0.0f);
+      } else {
+        const float4 w = lane < kCW ? sm.wpart[lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+        const float Mct = warp_max(w.x), Mcd = warp_max(w.z);
+        const float a = (w.y > 0.0f) ? w.y * ex2((w.x - Mct) * k) : 0.0f;
+        const float c = (w.w > 0.0f) ? w.w * ex2((w.z - Mcd) * k) : 0.0f;
+        rec = make_float4(Mct, warp_sum_lane0(a), Mcd, warp_sum_lane0(c));
+      }
+      const int rbad = __any_sync(kFull, lane < kCW && sm.wbad[lane]);
+      push_record4(smem_addr(&sm.xch1[par1][rank]), smem_addr(&sm.xbad1[par1][rank]),
+                   smem_addr(&sm.xbar1[par1]), rec, rbad, C, lane);
+      const bool arrived = mbar_wait_cluster(smem_addr(&sm.xbar1[par1]), ph1);
+      if (!arrived) set_status(P, sm, kStatusTimeout);
+      const float4 r = lane < C ? sm.xch1[par1][lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+      const int gbad = __any_sync(kFull, lane < C && sm.xbad1[par1][lane]) || !arrived;
+      if (kind == kArgmax) {
+        float v = lane < C ? r.x : -INFINITY;
+        int ii = lane < C ? __float_as_int(r.y) : INT_MAX;
+        warp_argmax(v, ii);
+        if (lane == 0) {
+          sm.bad = gbad || !(v > -INFINITY);
+          sm.cand = ii;
+          sm.acc = (p.i < p.gb) && (x == ii);
+        }
+      } else {
+        // Global max and normaliser of p (and q); the chunk-level CDF of p by an inclusive scan.
+        const float Mt = warp_max(r.x), Md = warp_max(r.z);
+        const float term_t = (lane < C && r.y > 0.0f) ? r.y * ex2((r.x - Mt) * k) : 0.0f;
+        const float incl_t = warp_incl_scan(term_t, lane);
+        const float St = __shfl_sync(kFull, incl_t, 31);
+        float excl_t = __shfl_up_sync(kFull, incl_t, 1);
+        if (lane == 0) excl_t = 0.0f;
+        bool b2 = gbad || !(Mt > -INFINITY && Mt < INFINITY);
+        float Sd = 1.0f;
+        if (kind == kVerify) {
+          const float term_d = (lane < C && r.w > 0.0f) ? r.w * ex2((r.z - Md) * k) : 0.0f;
+          Sd = __shfl_sync(kFull, warp_incl_scan(term_d, lane), 31);
+          b2 = b2 || !(Md > -INFINITY && Md < INFINITY);
+        }
+        // Chunk of a draw from p with threshold t (the bonus draw, or the residual fallback).
+        auto chunk_of = [&](float t, float& t_loc) -> int {
+          const unsigned hit = __ballot_sync(kFull, lane < C && term_t > 0.0f && incl_t > t);
+          const unsigned pos = __ballot_sync(kFull, lane < C && term_t > 0.0f);
+          const int c = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+          t_loc = t - __shfl_sync(kFull, excl_t, c);
+          return c;
+        };
+        float tl_b = 0.0f, tl_p = 0.0f;
+        const int cb_chunk = chunk_of(u_bon * St, tl_b);   // [R] One round, step 5
+        const int cp_chunk = chunk_of(u_res * St, tl_p);   // zero-residual fallback
+        if (lane == 0) {
+          const float ct = -fmaf(Mt, k, log2f(St));
+          const float cd = -fmaf(Md, k, log2f(Sd));
+          sm.k = k;
+          sm.cb = -Mt * k;
+          sm.ct = ct;
+          sm.cd = cd;
+          sm.bad = b2;
+          sm.acc = 1;
+          sm.px = sm.qx = 0.0f;
+          if (kind == kVerify) {
+            // [R] One round, step 3: keep x while u < min(1, p(x)/q(x)); q(x) = 0 keeps x.
+            const float px = ex2(fmaf(zx_t, k, ct));
+            const float qx = ex2(fmaf(zx_d, k, cd));
+            const float ratio = (qx > 0.0f) ? fminf(1.0f, __fdividef(px, qx)) : 1.0f;
+            sm.px = px;
+            sm.qx = qx;
+            sm.acc = u_acc < ratio;
+          }
+          sm.draw_chunk = (kind == kBonus) ? cb_chunk : -1;
+          sm.t_local = tl_b;
+          sm.draw_resid = 0;
+          sm.p_chunk = cp_chunk;
+          sm.p_tlocal = tl_p;
+        }
+      }
+      if (lane == 0) sm.stop_snap = sm.stop;
+    }
+    named_bar_sync(kConsumerBar, kCT);
+    if (sm.stop_snap) break;
+
+    if (kind == kArgmax) {
+      if (rank == 0 && cw == 0) {
+        const int acc = sm.acc;
+        const int flags = (sm.bad ? kFlagBad : 0) | (acc ? kFlagAccept : 0);
+        const float a = acc ? 1.0f : 0.0f;
+        finish_position(P, p.b, p.i, p.gb, sm.cand, flags, a, a, 1.0f, lane);
+      }
+      continue;
+    }
+
+    const float kk = sm.k, ct = sm.ct, cd = sm.cd, cb = sm.cb;
+    const int pbad = sm.bad;
+    float alpha = 0.0f;
+
+    if (kind == kVerify) {
+      // ---- pass 2: residual weights of the chunk, re-read from L2; one sum per vector ----
+      float W = 0.0f;
+      const f32x2 k2 = pk(kk, kk), c2 = pk(ct, cd);
+      const uint4* vt = reinterpret_cast<const uint4*>(rowt);
+      const uint4* vd = reinterpret_cast<const uint4*>(rowd);
+      int u = u0 + ctid;
+      for (; u + 3 * kCT < u1; u += 4 * kCT) {
+        uint4 t[4], d[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          t[j] = ld_stream_v4(vt + u + j * kCT);
+          d[j] = ld_stream_v4(vd + u + j * kCT);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float sv = resid_vec_sum<BF16>(t[j], d[j], k2, c2);
+          usum[u + j * kCT - u0] = sv;
+          W += sv;
+        }
+      }
+      for (; u < u1; u += kCT) {
+        const float sv = resid_vec_sum<BF16>(ld_stream_v4(vt + u), ld_stream_v4(vd + u), k2, c2);
+        usum[u - u0] = sv;
+        W += sv;
+      }
+      const float ws = warp_sum_lane0(W);
+      if (lane == 0) sm.wsum2[cw] = ws;
+      named_bar_sync(kConsumerBar, kCT);
+
+      // ---- exchange 2: residual chunk totals ----
+      const uint32_t par2 = e2 & 1, ph2 = (e2 >> 1) & 1;
+      ++e2;
+      if (cw == 0) {
+        const float wc = warp_sum_lane0(lane < kCW ? sm.wsum2[lane] : 0.0f);
+        if (lane < C) {
+          st_cluster_f32(map_to_rank(smem_addr(&sm.xch2[par2][rank]), lane), wc);
+          mbar_arrive_remote(map_to_rank(smem_addr(&sm.xbar2[par2]), lane));
+        }
+        const bool arrived = mbar_wait_cluster(smem_addr(&sm.xbar2[par2]), ph2);
+        if (!arrived) set_status(P, sm, kStatusTimeout);
+        const float w_r = lane < C ? sm.xch2[par2][lane] : 0.0f;
+        const float incl_w = warp_incl_scan(w_r, lane);
+        const float Wt = __shfl_sync(kFull, incl_w, 31);
+        float excl_w = __shfl_up_sync(kFull, incl_w, 1);
+        if (lane == 0) excl_w = 0.0f;
+        // Replacement from max(0, p - q) / sum max(0, p - q) ([R] One round, step 4): the chunk
+        // whose inclusive prefix first exceeds u * W (else, by rounding, the last positive chunk).
+        const float t = u_res * Wt;
+        const unsigned hit = __ballot_sync(kFull, lane < C && w_r > 0.0f && incl_w > t);
+        const unsigned pos = __ballot_sync(kFull, lane < C && w_r > 0.0f);
+        const int c = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+        const float tl = t - __shfl_sync(kFull, excl_w, c);
+        if (lane == 0) {
+          sm.alpha = fminf(1.0f, fmaxf(0.0f, 1.0f - Wt));
+          if (sm.acc) {
+            sm.draw_chunk = -1;
+          } else if (Wt > 0.0f) {
+            sm.draw_chunk = c;
+            sm.t_local = tl;
+            sm.draw_resid = 1;
+          } else {                                   // zero residual mass: draw from p
+            sm.draw_chunk = sm.p_chunk;
+            sm.t_local = sm.p_tlocal;
+            sm.draw_resid = 0;
+          }
+          sm.stop_snap = sm.stop;
+        }
+      }
+      named_bar_sync(kConsumerBar, kCT);
+      if (sm.stop_snap) break;
+      alpha = sm.alpha;
+    }
+
+    // ---- the draw and the position's finish ----
+    const int dchunk = sm.draw_chunk;
+    if (pbad || dchunk < 0) {
+      if (rank == 0 && cw == 0)
+        finish_position(P, p.b, p.i, p.gb, -1, pbad ? kFlagBad : kFlagAccept, alpha, sm.px, sm.qx,
+                        lane);
+      continue;
+    }
+    if (rank == dchunk) {
+      const bool resid = sm.draw_resid != 0;
+      const float tl = sm.t_local, px = sm.px, qx = sm.qx;
+      const int acc = sm.acc;
+      if (!resid) {
+        // Per-vector sums of p's weights exp2(z k + cb), re-read from L2.
+        const uint4* vt = reinterpret_cast<const uint4*>(rowt);
+        int u = u0 + ctid;
+        for (; u + 3 * kCT < u1; u += 4 * kCT) {
+          uint4 t[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) t[j] = ld_stream_v4(vt + u + j * kCT);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) usum[u + j * kCT - u0] = p_vec_sum<BF16>(t[j], kk, cb);
+        }
+        for (; u < u1; u += kCT) usum[u - u0] = p_vec_sum<BF16>(ld_stream_v4(vt + u), kk, cb);
+        named_bar_sync(kConsumerBar, kCT);
+      }
+      int finisher = 0;
+      const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, resid, kk, ct, cd, cb, sm, ctid,
+                                       finisher);
+      if (cw == finisher) {
+        const int flags = (tok < 0 ? kFlagBad : 0) | ((kind == kBonus || acc) ? kFlagAccept : 0);
+        finish_position(P, p.b, p.i, p.gb, tok, flags, alpha, px, qx, lane);
+      }
+    }
+  }
+
+  // ---- no CTA leaves while a peer may still write into its shared memory ----
+  if (cw == 0) {
+    if (lane < C) mbar_arrive_remote(map_to_rank(smem_addr(&sm.xdone), lane));
+    if (!mbar_wait_cluster(smem_addr(&sm.xdone), 0)) set_status(P, sm, kStatusTimeout);
+  }
+}
+
+const void* stream_fn(bool bf16) {
+  return bf16 ? reinterpret_cast<const void*>(sv_stream_kernel<true>)
+              : reinterpret_cast<const void*>(sv_stream_kernel<false>);
+}
+
+cudaError_t stream_attrs(const void* fn, int C) {
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBytes);
+  if (e != cudaSuccess) return e;
+  if (C > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+cudaLaunchConfig_t stream_config(int C, int nclusters, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nclusters * C), 1, 1);
+  cfg.blockDim = dim3(kThreadsS, 1, 1);
+  cfg.dynamicSmemBytes = kDynBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+}  // namespace
+
+cudaError_t stream_max_clusters(bool bf16, int C, int* n) {
+  const void* fn = stream_fn(bf16);
+  const cudaError_t e = stream_attrs(fn, C);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = stream_config(C, 64, nullptr, attr);
+  return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
+}
+
+cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream) {
+  const void* fn = stream_fn(bf16);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = stream_config(P.C, P.nclusters, stream, attr);
+  void* args[] = {&P};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace sv

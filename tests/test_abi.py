@@ -89,11 +89,10 @@ def test_argument_errors_are_host_side(L):
     assert call(L, ws=FAKE + 65544) == 5              # workspace needs 16 B
     assert call(L, ws=None) == 4                      # SV_ERR_WORKSPACE_TOO_SMALL
     assert call(L, wsb=16) == 4
-    # V too large for one cluster: bf16 rows whose length is not a multiple of 16 bytes use the
-    # element path (at most 16 * 512 * 8 logits); vector rows at most 16 * 512 * 8 vectors.
+    # Rows whose byte length is not a multiple of 16 take the element path, which holds at most
+    # 16 * 512 * 8 logits per row (16-byte rows stream and have no such limit).
     assert call(L, V=65537) == 2
-    assert call(L, V=16 * 512 * 8 * 8 + 8) == 2
-    assert call(L, dtype=0, V=16 * 512 * 8 * 4 + 4) == 2
+    assert call(L, dtype=0, V=65539) == 2
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

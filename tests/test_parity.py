@@ -256,12 +256,9 @@ def test_determinism_and_workspace_left_zeroed(sv):
         assert np.array_equal(x, y)
     from speculative_decoding_verification_55_gb300 import workspace_for, SV_DTYPE_BF16
     ws = workspace_for(w.B, w.G, w.V, SV_DTYPE_BF16, t["target_logits"].device)
-    assert int(ws.count_nonzero()) == 0 or _counters_zero(ws, w.B, w.G)
-
-
-def _counters_zero(ws, B, G):
-    rec = ((B * (G + 1) * 8 + 255) // 256) * 256
-    return int(ws[rec:rec + 4 * B].count_nonzero()) == 0
+    assert int(ws.count_nonzero()) == 0
+    from speculative_decoding_verification_55_gb300 import spec_verify_workspace_status
+    assert spec_verify_workspace_status(ws, w.B, w.G) == 0
 
 
 # ------------------------------------------------------------------------------------------------
