@@ -62,13 +62,17 @@ typedef enum {
   SV_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < spec_verify_workspace_size(...), or NULL   */
   SV_ERR_MISALIGNED = 5,          /* a pointer is not aligned to its element type (workspace: 16 B) */
   SV_ERR_CUDA = 6,                /* a CUDA runtime call failed (device query or launch)          */
-  SV_ERR_UNSUPPORTED_DEVICE = 7   /* the current device is not compute capability 10.3           */
+  SV_ERR_UNSUPPORTED_DEVICE = 7,  /* the current device is not compute capability 10.3           */
+  SV_ERR_SCRATCH_TOO_SMALL = 8    /* spec_verify_noalloc: the sizes need more scratch than
+                                     SV_NOALLOC_SCRATCH_BYTES                                     */
 } sv_status;
 
 typedef enum { SV_DTYPE_F32 = 0, SV_DTYPE_BF16 = 1 } sv_dtype;
 
 #define SV_MAX_GAMMA 64
 #define SV_VERSION 1
+/* Size of the library's static device scratch used by spec_verify_noalloc (1 MiB per device). */
+#define SV_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 /* Bytes of device workspace spec_verify needs for these sizes (per-position records, one arrival
  * counter per row and a status word), a multiple of 256. Returns 0 for invalid sizes.
@@ -117,6 +121,31 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
                    float* out_p_draft, float* out_q_draft,
                    int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                    void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* spec_verify_ex for callers that cannot allocate device memory. The pages have no counterpart:
+ * this is a deployment convenience, not part of the method.
+ *
+ * Who needs it: engines whose device memory is fully planned at start-up and that forbid any
+ * allocation on the serving path, host code that cannot afford the device-wide synchronisation of
+ * cudaMalloc, and plugin interfaces that hand over only the input and output buffers. They pass the
+ * same inputs and outputs as spec_verify_ex (the caller still owns those) but no workspace: the
+ * kernels' scratch lives in a static device array of SV_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits. The call allocates nothing
+ * and frees nothing.
+ *
+ * Limit: sizes whose spec_verify_workspace_size(B, gamma_max, V, dtype) exceeds
+ * SV_NOALLOC_SCRATCH_BYTES are rejected with SV_ERR_SCRATCH_TOO_SMALL before anything is enqueued.
+ * Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture. Each call clears the
+ * scratch's counters on `cuda_stream` before its launch. Every call shares the one array: calls
+ * whose executions overlap on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller. Arguments, layout and errors otherwise as in spec_verify_ex. */
+int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const int32_t* draft_len,
+                        const float* temperature, const float* uniforms, int32_t* out_tokens,
+                        int32_t* out_num_emitted, float* out_alpha, float* out_p_draft,
+                        float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                        void* cuda_stream);
 
 /* Reads the workspace's sticky status word into *status_out after synchronising `cuda_stream`
  * (B and gamma_max as in the call that used the workspace). 0 means every call so far completed

@@ -4,7 +4,9 @@ The work runs in libspecverify.so (hand-written sm_103a CUDA behind the C ABI of
 include/spec_verify.h); this package is its thin ctypes binding.
 """
 from ._binding import (SV_DTYPE_BF16, SV_DTYPE_F32, SV_MAX_GAMMA, SV_OK, SpecVerifyError,  # noqa: F401
-                       lib, spec_verify, spec_verify_ex, spec_verify_status_string,
+                       SV_ERR_SCRATCH_TOO_SMALL, SV_NOALLOC_SCRATCH_BYTES,
+                       lib, spec_verify, spec_verify_ex, spec_verify_noalloc,
+                       spec_verify_status_string,
                        spec_verify_version, spec_verify_workspace_size,
                        spec_verify_workspace_status, verify, workspace_for)
 from .build import LIB_PATH, build_library  # noqa: F401

@@ -19,10 +19,12 @@ SV_MAX_GAMMA = 64
 STATUS_NAMES = {
     0: "SV_OK", 1: "SV_ERR_NULL_POINTER", 2: "SV_ERR_BAD_SHAPE", 3: "SV_ERR_BAD_DTYPE",
     4: "SV_ERR_WORKSPACE_TOO_SMALL", 5: "SV_ERR_MISALIGNED", 6: "SV_ERR_CUDA",
-    7: "SV_ERR_UNSUPPORTED_DEVICE",
+    7: "SV_ERR_UNSUPPORTED_DEVICE", 8: "SV_ERR_SCRATCH_TOO_SMALL",
 }
+SV_ERR_SCRATCH_TOO_SMALL = 8
+SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
-EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_workspace_size",
+EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_workspace_size",
             "spec_verify_workspace_status", "spec_verify_status_string", "spec_verify_version")
 
 _lib = None
@@ -53,6 +55,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify.restype = ctypes.c_int
             L.spec_verify_ex.argtypes = common + [f32p, f32p] + tail
             L.spec_verify_ex.restype = ctypes.c_int
+            L.spec_verify_noalloc.argtypes = common + [f32p, f32p, i32, i32, i32, i32, vp]
+            L.spec_verify_noalloc.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
             L.spec_verify_workspace_size.restype = ctypes.c_size_t
             L.spec_verify_workspace_status.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int32), vp]
@@ -154,6 +158,36 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, tempera
         _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_ex")
+
+
+def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, draft_len, temperature,
+                        uniforms, out_tokens, out_num_emitted, out_alpha, out_p_draft=None,
+                        out_q_draft=None, stream=None) -> None:
+    """Calls the C ABI spec_verify_noalloc: like spec_verify_ex, with the library's static device
+    scratch instead of a workspace (for callers that cannot allocate). Raises SpecVerifyError on a
+    nonzero status, e.g. SV_ERR_SCRATCH_TOO_SMALL for sizes beyond SV_NOALLOC_SCRATCH_BYTES."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    _check(target_logits, "target_logits", device=dev)
+    _check(draft_logits, "draft_logits", dtype=target_logits.dtype, shape=(B, G, V), device=dev)
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, G), dev)
+    _check(draft_len, "draft_len", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, G + 2), dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B, G + 1), dev)
+    _check(out_num_emitted, "out_num_emitted", torch.int32, (B,), dev)
+    for name, t in (("out_alpha", out_alpha), ("out_p_draft", out_p_draft),
+                    ("out_q_draft", out_q_draft)):
+        _check(t, name, torch.float32, (B, G), dev)
+    st = lib().spec_verify_noalloc(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
+        _ptr(temperature), _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted),
+        _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
+        B, G, V, _dtype_code(target_logits), _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_noalloc")
 
 
 def spec_verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,

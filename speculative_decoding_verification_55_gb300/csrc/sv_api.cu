@@ -117,6 +117,9 @@ const char* spec_verify_status_string(int status) {
     case SV_ERR_MISALIGNED: return "SV_ERR_MISALIGNED: a pointer is not aligned to its element type";
     case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA runtime call failed";
     case SV_ERR_UNSUPPORTED_DEVICE: return "SV_ERR_UNSUPPORTED_DEVICE: the device is not sm_103";
+    case SV_ERR_SCRATCH_TOO_SMALL:
+      return "SV_ERR_SCRATCH_TOO_SMALL: the sizes need more than the library's static scratch "
+             "(SV_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown sv_status";
   }
 }
