@@ -3,8 +3,8 @@
 //
 // Work split. A position (b, i) of the batch is one target row (plus the draft row for a drafted
 // position) of V logits. Each cluster of C CTAs owns every nclusters-th position slot; CTA r of the
-// cluster owns the r-th contiguous chunk of every row it touches. Two CTAs share an SM, so one
-// CTA's exchanges and barriers overlap the other's arithmetic. A CTA is 8 consumer warps and one
+// cluster owns the r-th contiguous chunk of every row it touches. Four CTAs share an SM, so one
+// CTA's exchanges and barriers overlap the others' arithmetic. A CTA is 4 consumer warps and one
 // producer warp.
 //
 // Producer warp (one thread). Walks the cluster's positions and streams this CTA's chunks through a
@@ -12,20 +12,25 @@
 // mbarrier pair per slot. It runs ahead of the consumers by the ring's capacity, so HBM keeps
 // streaming while the consumers exchange partial results.
 //
+// One cluster exchange per position: after pass 1 of position n, every CTA pushes its softmax
+// partials of n together with its residual total of the previous drafted position (st.async into
+// every peer's shared memory, completing bytes on the peer's mbarrier). The previous position's
+// alpha, draw and finish follow that exchange; position n's own residual pass follows it too, and
+// n's totals ride on the next exchange.
+//
 // Consumer warps, per position:
 //   pass 1   online softmax of the chunk straight out of the ring: running max (with a
 //            NaN-propagating tracker beside it) and sum of exp2((z - m) log2(e) / T); greedy rows:
 //            running argmax with the lowest index.
-//   xchg 1   CTA partials are pushed into every CTA of the cluster (st.shared::cluster) with a remote
-//            mbarrier arrival; each CTA combines the C records in the same fixed order: global max
-//            M, normaliser S (an inclusive scan over ranks = the chunk-level CDF of p), the accept
-//            test u < min(1, p(x)/q(x)), the chunk that holds a bonus-draw threshold.
+//   xchg     each CTA combines the C records in the same fixed order: global max M, normaliser S
+//            (an inclusive scan over ranks = the chunk-level CDF of p), the accept test
+//            u < min(1, p(x)/q(x)), the chunk that holds a bonus-draw threshold.
 //   pass 2   (drafted positions) the chunk again, now from L2 where pass 1 left it: residual
 //            weights max(0, p - q), p and q normalised inside the exponent; one sum per 16-byte
 //            vector is kept in shared memory for the draw. alpha = 1 - W with W the residual mass:
 //            sum min(p, q) + sum max(0, p - q) = sum p = 1 ([R] Why the output is exactly the
 //            target's).
-//   xchg 2   residual chunk totals (inclusive scan over ranks).
+//   next     the residual chunk totals (inclusive scan over ranks) arrive with the next exchange.
 //   draw     the CTA whose chunk holds the inverse-CDF threshold scans its per-vector sums in index
 //            order (block-wide prefix sum), reloads the one vector that crosses the threshold and
 //            picks the token inside it. A bonus draw first fills the per-vector sums of p from L2.
@@ -43,12 +48,24 @@
 namespace sv {
 namespace {
 
-constexpr int kCW = 8;                        // consumer warps
+// Four CTAs per SM, each 4 consumer warps + 1 producer warp with a 2 x 16 KB ring: four
+// independent position streams per SM, so one CTA's exchange waits overlap another's arithmetic.
+#ifndef SV_STREAM_CONSUMER_WARPS
+#define SV_STREAM_CONSUMER_WARPS 4
+#endif
+#ifndef SV_STREAM_RING_SLOTS
+#define SV_STREAM_RING_SLOTS 2
+#endif
+#ifndef SV_STREAM_CTAS_PER_SM
+#define SV_STREAM_CTAS_PER_SM 4
+#endif
+constexpr int kCW = SV_STREAM_CONSUMER_WARPS;   // consumer warps
 constexpr int kCT = kCW * 32;                 // consumer threads
 constexpr int kThreadsS = kCT + 32;           // plus the producer warp
 constexpr int kSlotBytes = 16384;
 constexpr int kSlotUnits = kSlotBytes / 16;
-constexpr int kNumSlots = 5;
+constexpr int kNumSlots = SV_STREAM_RING_SLOTS;
+static_assert(kSlotUnits % kCT == 0, "a ring slot splits evenly over the consumer threads");
 constexpr int kRingBytes = kSlotBytes * kNumSlots;
 constexpr int kDynBytes = kRingBytes + kStreamMaxUnits * 4;   // ring + per-vector sums
 constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
@@ -58,12 +75,10 @@ enum : unsigned { kStatusTimeout = 1u };
 struct Shared {
   uint64_t full[kNumSlots];
   uint64_t empty[kNumSlots];
-  uint64_t xbar1[2];                 // exchange 1 arrivals (one per CTA), by exchange parity
-  uint64_t xbar2[2];                 // exchange 2 arrivals
+  uint64_t xbar[2];                  // exchange: bytes pushed by every CTA complete it, by parity
   uint64_t xdone;                    // end-of-kernel arrivals
-  float4 xch1[2][kMaxCluster];       // records pushed by every rank, exchange 1
-  int xbad1[2][kMaxCluster];
-  float xch2[2][kMaxCluster];        // residual chunk totals, exchange 2
+  float4 xrec[2][kMaxCluster];       // per rank: (m_p, s_p, m_q, s_q), or (argmax value, index)
+  uint2 xaux[2][kMaxCluster];        // per rank: (bad flag, residual total of the pending position)
   float4 wpart[kCW];                 // warp partials
   int wbad[kCW];
   int widx[kCW];
@@ -72,12 +87,16 @@ struct Shared {
   int scan_slot[kCW];
   int stop;                          // set by any thread that gave up a wait
   int stop_snap;                     // its value as published by consumer warp 0 under a barrier
-  // per-position broadcast from consumer warp 0
+  // broadcast from consumer warp 0 after an exchange: the current position ...
   float k, ct, cd, cb;               // log2(e)/T; exponent offsets of p, q and of unnormalised p
-  float px, qx, alpha, t_local;
-  int acc, bad, cand, draw_chunk, draw_resid;
-  int p_chunk;                       // chunk of a draw from p with the residual uniform
-  float p_tlocal;
+  float px, qx, t_local, p_tlocal;
+  int acc, bad, cand, draw_chunk, p_chunk;
+  // ... and the pending drafted position whose residual totals this exchange carried
+  float pend_alpha, pend_tlocal;
+  int pend_chunk, pend_resid;
+  // the draw's crossing vector, handed from the thread that found it to the finishing warp
+  int dj, dover;
+  float dbefore;
 };
 
 struct Pos {
@@ -86,11 +105,13 @@ struct Pos {
   bool len_ok, t_ok, greedy, load, two;
 };
 
+// Slot s in position-major order (s = i * B + b): the slots a cluster strides over mix every
+// position index, so ragged rows (fewer positions at large i) and the cheaper bonus positions
+// spread evenly over the clusters.
 __device__ __forceinline__ Pos classify(const Params& P, int s) {
   Pos p;
-  const int G1 = P.G + 1;
-  p.b = s / G1;
-  p.i = s - p.b * G1;
+  p.i = s / P.B;
+  p.b = s - p.i * P.B;
   p.gb = P.draft_len ? __ldg(P.draft_len + p.b) : P.G;
   p.T = __ldg(P.temperature + p.b);
   p.len_ok = p.gb >= 0 && p.gb <= P.G;
@@ -135,6 +156,54 @@ __device__ __forceinline__ void online_update(const uint4& v, float k, float& m,
     s = add2(s, pk(ex2(a0), ex2(a1)));
     s = add2(s, pk(ex2(a2), ex2(a3)));
   }
+}
+
+// Pass-1 update with the kUnitsPerSlot vectors one thread takes from a ring slot: one max and one
+// rescale check for the batch, then every exp2 with two independent accumulators.
+template <bool BF16, int N>
+__device__ __forceinline__ void online_update_batch(const uint4 (&v)[N], float k, float& m, f32x2& s,
+                                                    float& mx) {
+  float vm = -INFINITY;
+  if (BF16) {
+    uint32_t a = bmax2_nan(bmax2_nan(v[0].x, v[0].y), bmax2_nan(v[0].z, v[0].w));
+#pragma unroll
+    for (int j = 1; j < N; ++j)
+      a = bmax2_nan(a, bmax2_nan(bmax2_nan(v[j].x, v[j].y), bmax2_nan(v[j].z, v[j].w)));
+    vm = max_nan(bf_lo(a), bf_hi(a));
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) vm = max_nan(vm, vec_max<false>(v[j]));
+  }
+  mx = max_nan(mx, vm);
+  if (vm > m) {                                   // rescale the running sum to the new max
+    float s0, s1;
+    upk(s, s0, s1);
+    const float f = ex2((m - vm) * k);
+    s = pk(s0 * f, s1 * f);
+    m = vm;
+  }
+  const float c = -m * k;
+  const f32x2 k2 = pk(k, k), c2 = pk(c, c);
+  f32x2 s2 = pk(0.0f, 0.0f);
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+    for (int q = 0; q < 4; q += 2) {
+      float a0, a1, b0, b1;
+      if (BF16) {
+        upk(fma2(pk(bf_lo(w[q]), bf_hi(w[q])), k2, c2), a0, a1);
+        upk(fma2(pk(bf_lo(w[q + 1]), bf_hi(w[q + 1])), k2, c2), b0, b1);
+        s = add2(s, pk(ex2(a0), ex2(a1)));
+        s2 = add2(s2, pk(ex2(b0), ex2(b1)));
+      } else {
+        upk(fma2(pk(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), k2, c2), a0, a1);
+        if (q == 0) s = add2(s, pk(ex2(a0), ex2(a1)));
+        else s2 = add2(s2, pk(ex2(a0), ex2(a1)));
+      }
+    }
+  }
+  s = add2(s, s2);
 }
 
 // Pass-1 greedy update: running max and the lowest index holding it.
@@ -233,15 +302,10 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
     best_j = max(best_j, sm.widx[w2]);
   }
   // The crossing vector and the weight before it (winner thread), else the last positive vector.
-  finisher = (win == INT_MAX) ? 0 : (win >> 5);
-  if (cw != finisher) return -1;
-  int vj = -1;
-  float before = 0.0f;
-  bool overrun = (win == INT_MAX);
-  if (!overrun && ctid == win) {
+  if (win != INT_MAX && ctid == win) {
     float c = wexcl + excl;
-    int lastpos = -1;
-    float c_last = c;
+    int lastpos = -1, vj = -1;
+    float c_last = c, before = 0.0f;
     for (int j = r0; j < r1; ++j) {
       const float v = usum[j];
       if (v > 0.0f) {
@@ -255,16 +319,21 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
         c += v;
       }
     }
-    if (vj < 0) {          // rounding: the run's sums crossed, its vectors did not
-      vj = lastpos;
-      before = c_last;
-      overrun = true;
-    }
+    const bool over = vj < 0;        // rounding: the run's sums crossed, its vectors did not
+    sm.dj = over ? lastpos : vj;
+    sm.dbefore = over ? c_last : before;
+    sm.dover = over;
+  } else if (win == INT_MAX && ctid == 0) {
+    sm.dj = best_j;
+    sm.dbefore = 0.0f;
+    sm.dover = 1;
   }
-  const int src = overrun && win == INT_MAX ? 0 : (win & 31);
-  vj = overrun && win == INT_MAX ? best_j : __shfl_sync(kFull, vj, src);
-  before = __shfl_sync(kFull, before, src);
-  overrun = __shfl_sync(kFull, overrun ? 1 : 0, src) != 0;
+  named_bar_sync(kConsumerBar, kCT);   // after this no thread reads usum: the caller may reuse it
+  finisher = (win == INT_MAX) ? 0 : (win >> 5);
+  if (cw != finisher) return -1;
+  const int vj = sm.dj;
+  const float before = sm.dbefore;
+  const bool overrun = sm.dover != 0;
   int tok = -1;
   if (lane == 0 && vj >= 0) {
     const int u = u0 + vj;
@@ -299,19 +368,11 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
   return __shfl_sync(kFull, tok, 0);
 }
 
-// Lane r < C of the calling warp pushes a record into CTA r's slot `slot_addr` (same offset in every
-// CTA) and arrives on CTA r's barrier.
-__device__ __forceinline__ void push_record4(uint32_t slot_addr, uint32_t bad_addr, uint32_t bar,
-                                             float4 v, int bad, int C, int lane) {
-  if (lane < C) {
-    st_cluster_v4f32(map_to_rank(slot_addr, lane), v.x, v.y, v.z, v.w);
-    st_cluster_s32(map_to_rank(bad_addr, lane), bad);
-    mbar_arrive_remote(map_to_rank(bar, lane));
-  }
-}
+// Bytes every CTA pushes into every CTA of its cluster per exchange: one float4 record and one uint2.
+constexpr uint32_t kXchBytes = 24;
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Shared sm;
   constexpr size_t ES = BF16 ? 2 : 4;
@@ -334,10 +395,7 @@ __global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P)
       mbar_init(smem_addr(&sm.full[s]), 1);
       mbar_init(smem_addr(&sm.empty[s]), kCW);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&sm.xbar1[s]), C);
-      mbar_init(smem_addr(&sm.xbar2[s]), C);
-    }
+    for (int s = 0; s < 2; ++s) mbar_init(smem_addr(&sm.xbar[s]), 1);
     mbar_init(smem_addr(&sm.xdone), C);
     sm.stop = 0;
     sm.stop_snap = 0;
@@ -386,121 +444,76 @@ __global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P)
   const int ctid = tid;          // 0 .. kCT-1
   const int cw = warp;
   uint32_t tc = 0;               // ring slots consumed
-  uint32_t e1 = 0, e2 = 0;       // exchanges done
+  uint32_t ex = 0;               // exchanges done
   const uint4* ringv = reinterpret_cast<const uint4*>(dyn);
 
-  for (int s = cid; s < total; s += P.nclusters) {
-    const Pos p = classify(P, s);
-    if (!p.load) {
-      if (!(p.len_ok && p.t_ok) && p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
-      continue;
-    }
-    const bool ok = row_scalars_ok(P, p.b, p.gb, p.greedy, lane);
-    const int kind = p.greedy ? kArgmax : (p.two ? kVerify : kBonus);
-    const char* rowt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES;
-    const char* rowd = p.two ? static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES
-                             : nullptr;
-    const int x = p.i < p.gb ? __ldg(P.tokens + (size_t)p.b * G + p.i) : -1;
+  // The pending drafted position: pass 2 done, its residual chunk totals ride on the next exchange,
+  // after which its draw (if rejected) and finish happen. Uniform across the cluster.
+  bool pv = false;
+  int pb = 0, pi = 0, pgb = 0, pacc = 1, pbad = 0;
+  const char* prt = nullptr;
+  const char* prd = nullptr;
+  float pkk = 0.0f, pct = 0.0f, pcd = 0.0f, pcb = 0.0f, ppx = 0.0f, pqx = 0.0f;
+  int pp_chunk = 0;                          // pending: chunk of the fallback draw from p
+  float pp_tlocal = 0.0f;
+  float pu_res = 0.0f;                       // consumer warp 0: the pending residual uniform
 
-    // Early scalar loads for the accept test (their latency hides behind pass 1).
-    float zx_t = 0.0f, zx_d = 0.0f, u_acc = 0.0f, u_res = 0.0f, u_bon = 0.0f;
-    if (ok && cw == 0 && !p.greedy) {
-      const float* ur = P.uniforms + (size_t)p.b * (G + 2);
-      u_res = __ldg(ur + G);
-      u_bon = __ldg(ur + G + 1);
-      if (kind == kVerify) {
-        u_acc = __ldg(ur + p.i);
-        zx_t = load_logit<BF16>(rowt, x);
-        zx_d = load_logit<BF16>(rowd, x);
-      }
+  // Per-vector sums of p's unnormalised weights exp2(z k + cb) of this CTA's chunk, from L2.
+  auto fill_p_sums = [&](const char* rt, float kk, float cbv) {
+    const uint4* vt = reinterpret_cast<const uint4*>(rt);
+    int u = u0 + ctid;
+    for (; u + 3 * kCT < u1; u += 4 * kCT) {
+      uint4 t[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[j] = ld_stream_v4(vt + u + j * kCT);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) usum[u + j * kCT - u0] = p_vec_sum<BF16>(t[j], kk, cbv);
     }
+    for (; u < u1; u += kCT) usum[u - u0] = p_vec_sum<BF16>(ld_stream_v4(vt + u), kk, cbv);
+  };
 
-    // ---- pass 1 out of the ring ----
-    const float k = p.greedy ? 0.0f : kLog2e / p.T;
-    float mt = -INFINITY, md = -INFINITY, mxt = -INFINITY, mxd = -INFINITY;
-    f32x2 st = pk(0.0f, 0.0f), sd = pk(0.0f, 0.0f);
-    int idx = INT_MAX;
-    bool timed_out = false;
-    for (int row = 0; row < (p.two ? 2 : 1); ++row) {
-      for (int ks = 0; ks < nsl; ++ks, ++tc) {
-        const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
-        if (!mbar_wait(smem_addr(&sm.full[slot]), par)) timed_out = true;
-        const int nu = min(kSlotUnits, cu - ks * kSlotUnits);
-        const uint4* src = ringv + slot * kSlotUnits;
-        if (ok && !timed_out) {
-          if (kind == kArgmax) {
-            for (int uu = ctid; uu < nu; uu += kCT)
-              argmax_update<BF16>(src[uu], (u0 + ks * kSlotUnits + uu) * E, mt, idx, mxt);
-          } else if (row == 0) {
-            for (int uu = ctid; uu < nu; uu += kCT) online_update<BF16>(src[uu], k, mt, st, mxt);
-          } else {
-            for (int uu = ctid; uu < nu; uu += kCT) online_update<BF16>(src[uu], k, md, sd, mxd);
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
-      }
-    }
-    if (timed_out) set_status(P, sm, kStatusTimeout);
-    if (!ok) {                       // drafted token or uniform out of range: the row is an error
-      if (p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
-      continue;
-    }
-
-    // ---- warp partials ----
-    if (kind == kArgmax) {
-      warp_argmax(mt, idx);
-      const int bad = __any_sync(kFull, (mxt != mxt) || mxt == INFINITY);
-      if (lane == 0) {
-        sm.wpart[cw] = make_float4(mt, 0.0f, 0.0f, 0.0f);
-        sm.widx[cw] = idx;
-        sm.wbad[cw] = bad;
-      }
-    } else {
-      float s0, s1;
-      upk(st, s0, s1);
-      float sT = s0 + s1;
-      upk(sd, s0, s1);
-      float sD = s0 + s1;
-      const float Mwt = warp_max(mt), Mwd = warp_max(md);
-      sT = (sT > 0.0f) ? sT * ex2((mt - Mwt) * k) : 0.0f;
-      sD = (sD > 0.0f) ? sD * ex2((md - Mwd) * k) : 0.0f;
-      sT = warp_sum_lane0(sT);
-      sD = warp_sum_lane0(sD);
-      const float mxa = max_nan(mxt, mxd);
-      const int bad = __any_sync(kFull, (mxa != mxa) || mxa == INFINITY);
-      if (lane == 0) {
-        sm.wpart[cw] = make_float4(Mwt, sT, Mwd, sD);
-        sm.wbad[cw] = bad;
-      }
-    }
-    named_bar_sync(kConsumerBar, kCT);
-
-    // ---- exchange 1 (consumer warp 0) ----
-    const uint32_t par1 = e1 & 1, ph1 = (e1 >> 1) & 1;
-    ++e1;
+  // One cluster exchange (consumer warp 0 pushes and combines; every consumer thread calls it).
+  // It carries the current position's pass-1 partials (has_cur) and the pending position's
+  // residual total (pv), and broadcasts the combined results through shared memory.
+  auto exchange = [&](bool has_cur, int kind, const Pos& p, int x, float k, float zx_t, float zx_d,
+                      float u_acc, float u_res, float u_bon) {
+    const uint32_t par = ex & 1, ph = (ex >> 1) & 1;
+    ++ex;
     if (cw == 0) {
-      float4 rec;
-      if (kind == kArgmax) {
-        float v = lane < kCW ? sm.wpart[lane].x : -INFINITY;
-        int ii = lane < kCW ? sm.widx[lane] : INT_MAX;
-        warp_argmax(v, ii);
-        rec = make_float4(v, __int_as_float(ii), 0.0f, 0.0f);
-      } else {
-        const float4 w = lane < kCW ? sm.wpart[lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
-        const float Mct = warp_max(w.x), Mcd = warp_max(w.z);
-        const float a = (w.y > 0.0f) ? w.y * ex2((w.x - Mct) * k) : 0.0f;
-        const float c = (w.w > 0.0f) ? w.w * ex2((w.z - Mcd) * k) : 0.0f;
-        rec = make_float4(Mct, warp_sum_lane0(a), Mcd, warp_sum_lane0(c));
+      // The pending position's CTA residual total (its warp partials are ordered by the barrier
+      // every consumer passed before this exchange).
+      const float pw = pv ? warp_sum_lane0(lane < kCW ? sm.wsum2[lane] : 0.0f) : 0.0f;
+      float4 rec = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+      int rbad = 0;
+      if (has_cur) {
+        if (kind == kArgmax) {
+          float v = lane < kCW ? sm.wpart[lane].x : -INFINITY;
+          int ii = lane < kCW ? sm.widx[lane] : INT_MAX;
+          warp_argmax(v, ii);
+          rec = make_float4(v, __int_as_float(ii), 0.0f, 0.0f);
+        } else {
+          const float4 w = lane < kCW ? sm.wpart[lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+          const float Mct = warp_max(w.x), Mcd = warp_max(w.z);
+          const float a = (w.y > 0.0f) ? w.y * ex2((w.x - Mct) * k) : 0.0f;
+          const float c = (w.w > 0.0f) ? w.w * ex2((w.z - Mcd) * k) : 0.0f;
+          rec = make_float4(Mct, warp_sum_lane0(a), Mcd, warp_sum_lane0(c));
+        }
+        rbad = __any_sync(kFull, lane < kCW && sm.wbad[lane]);
       }
-      const int rbad = __any_sync(kFull, lane < kCW && sm.wbad[lane]);
-      push_record4(smem_addr(&sm.xch1[par1][rank]), smem_addr(&sm.xbad1[par1][rank]),
-                   smem_addr(&sm.xbar1[par1]), rec, rbad, C, lane);
-      const bool arrived = mbar_wait_cluster(smem_addr(&sm.xbar1[par1]), ph1);
+      if (lane < C) {
+        const uint32_t bar_r = map_to_rank(smem_addr(&sm.xbar[par]), lane);
+        st_async_v4(map_to_rank(smem_addr(&sm.xrec[par][rank]), lane), __float_as_uint(rec.x),
+                    __float_as_uint(rec.y), __float_as_uint(rec.z), __float_as_uint(rec.w), bar_r);
+        st_async_v2(map_to_rank(smem_addr(&sm.xaux[par][rank]), lane), rbad ? 1u : 0u,
+                    __float_as_uint(pw), bar_r);
+      }
+      if (lane == 0) mbar_arrive_expect_tx(smem_addr(&sm.xbar[par]), kXchBytes * C);
+      const bool arrived = mbar_wait_cluster(smem_addr(&sm.xbar[par]), ph);
       if (!arrived) set_status(P, sm, kStatusTimeout);
-      const float4 r = lane < C ? sm.xch1[par1][lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
-      const int gbad = __any_sync(kFull, lane < C && sm.xbad1[par1][lane]) || !arrived;
-      if (kind == kArgmax) {
+      const float4 r = lane < C ? sm.xrec[par][lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
+      const uint2 au = lane < C ? sm.xaux[par][lane] : make_uint2(0u, 0u);
+      const int gbad = __any_sync(kFull, au.x != 0u) || !arrived;
+      if (has_cur && kind == kArgmax) {
         float v = lane < C ? r.x : -INFINITY;
         int ii = lane < C ? __float_as_int(r.y) : INT_MAX;
         warp_argmax(v, ii);
@@ -509,7 +522,7 @@ __global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P)
           sm.cand = ii;
           sm.acc = (p.i < p.gb) && (x == ii);
         }
-      } else {
+      } else if (has_cur) {
         // Global max and normaliser of p (and q); the chunk-level CDF of p by an inclusive scan.
         const float Mt = warp_max(r.x), Md = warp_max(r.z);
         const float term_t = (lane < C && r.y > 0.0f) ? r.y * ex2((r.x - Mt) * k) : 0.0f;
@@ -556,15 +569,166 @@ __global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P)
           }
           sm.draw_chunk = (kind == kBonus) ? cb_chunk : -1;
           sm.t_local = tl_b;
-          sm.draw_resid = 0;
           sm.p_chunk = cp_chunk;
           sm.p_tlocal = tl_p;
+        }
+      }
+      if (pv) {
+        // The pending position's residual mass W and alpha = 1 - W; on a rejection, the chunk whose
+        // inclusive prefix first exceeds u * W ([R] One round, step 4), else (rounding) the last
+        // positive chunk; with no residual mass at all, the draw from p picked at its exchange.
+        const float w_r = lane < C ? __uint_as_float(au.y) : 0.0f;
+        const float incl_w = warp_incl_scan(w_r, lane);
+        const float Wt = __shfl_sync(kFull, incl_w, 31);
+        float excl_w = __shfl_up_sync(kFull, incl_w, 1);
+        if (lane == 0) excl_w = 0.0f;
+        const float t = pu_res * Wt;
+        const unsigned hit = __ballot_sync(kFull, lane < C && w_r > 0.0f && incl_w > t);
+        const unsigned pos = __ballot_sync(kFull, lane < C && w_r > 0.0f);
+        const int c = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
+        const float tl = t - __shfl_sync(kFull, excl_w, c);
+        if (lane == 0) {
+          sm.pend_alpha = fminf(1.0f, fmaxf(0.0f, 1.0f - Wt));
+          sm.pend_chunk = (pacc || pbad) ? -1 : (Wt > 0.0f ? c : -2);
+          sm.pend_tlocal = tl;
+          sm.pend_resid = Wt > 0.0f;
         }
       }
       if (lane == 0) sm.stop_snap = sm.stop;
     }
     named_bar_sync(kConsumerBar, kCT);
+  };
+
+  // Draw (if rejected) and finish of the pending position; every consumer thread calls it.
+  auto finish_pending = [&]() {
+    if (!pv) return;
+    pv = false;
+    int dch = sm.pend_chunk;
+    const float alpha = sm.pend_alpha;
+    bool resid = sm.pend_resid != 0;
+    float tl = sm.pend_tlocal;
+    if (dch == -2) {                 // zero residual mass: draw from p with the residual uniform
+      dch = pp_chunk;
+      tl = pp_tlocal;
+      resid = false;
+    }
+    if (dch < 0) {
+      if (rank == 0 && cw == 0)
+        finish_position(P, pb, pi, pgb, -1, pbad ? kFlagBad : kFlagAccept, alpha, ppx, pqx, lane);
+      return;
+    }
+    if (rank != dch) return;
+    if (!resid) {
+      fill_p_sums(prt, pkk, pcb);
+      named_bar_sync(kConsumerBar, kCT);
+    }
+    int finisher = 0;
+    const int tok = chunk_draw<BF16>(usum, cu, u0, tl, prt, prd, resid, pkk, pct, pcd, pcb, sm, ctid,
+                                     finisher);
+    if (cw == finisher) finish_position(P, pb, pi, pgb, tok, tok < 0 ? kFlagBad : 0, alpha, ppx, pqx,
+                                        lane);
+  };
+
+  for (int s = cid; s < total; s += P.nclusters) {
+    const Pos p = classify(P, s);
+    if (!p.load) {
+      if (!(p.len_ok && p.t_ok) && p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
+      continue;
+    }
+    const bool ok = row_scalars_ok(P, p.b, p.gb, p.greedy, lane);
+    const int kind = p.greedy ? kArgmax : (p.two ? kVerify : kBonus);
+    const char* rowt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES;
+    const char* rowd = p.two ? static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES
+                             : nullptr;
+    const int x = p.i < p.gb ? __ldg(P.tokens + (size_t)p.b * G + p.i) : -1;
+
+    // Early scalar loads for the accept test (their latency hides behind pass 1).
+    float zx_t = 0.0f, zx_d = 0.0f, u_acc = 0.0f, u_res = 0.0f, u_bon = 0.0f;
+    if (ok && cw == 0 && !p.greedy) {
+      const float* ur = P.uniforms + (size_t)p.b * (G + 2);
+      u_res = __ldg(ur + G);
+      u_bon = __ldg(ur + G + 1);
+      if (kind == kVerify) {
+        u_acc = __ldg(ur + p.i);
+        zx_t = load_logit<BF16>(rowt, x);
+        zx_d = load_logit<BF16>(rowd, x);
+      }
+    }
+
+    // ---- pass 1 out of the ring ----
+    const float k = p.greedy ? 0.0f : kLog2e / p.T;
+    float mt = -INFINITY, md = -INFINITY, mxt = -INFINITY, mxd = -INFINITY;
+    f32x2 st = pk(0.0f, 0.0f), sd = pk(0.0f, 0.0f);
+    int idx = INT_MAX;
+    bool timed_out = false;
+    for (int row = 0; row < (p.two ? 2 : 1); ++row) {
+      for (int ks = 0; ks < nsl; ++ks, ++tc) {
+        const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
+        if (!mbar_wait(smem_addr(&sm.full[slot]), par)) timed_out = true;
+        const int nu = min(kSlotUnits, cu - ks * kSlotUnits);
+        const uint4* src = ringv + slot * kSlotUnits;
+        if (ok && !timed_out) {
+          constexpr int N = kSlotUnits / kCT;
+          const uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
+          uint4 v[N];
+#pragma unroll
+          for (int j = 0; j < N; ++j) {
+            const int uu = ctid + j * kCT;
+            v[j] = uu < nu ? src[uu] : make_uint4(ninf, ninf, ninf, ninf);
+          }
+          if (kind == kArgmax) {
+#pragma unroll
+            for (int j = 0; j < N; ++j)
+              argmax_update<BF16>(v[j], (u0 + ks * kSlotUnits + ctid + j * kCT) * E, mt, idx, mxt);
+          } else if (row == 0) {
+            online_update_batch<BF16, N>(v, k, mt, st, mxt);
+          } else {
+            online_update_batch<BF16, N>(v, k, md, sd, mxd);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+      }
+    }
+    if (timed_out) set_status(P, sm, kStatusTimeout);
+    if (!ok) {                       // drafted token or uniform out of range: the row is an error
+      if (p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
+      continue;
+    }
+
+    // ---- warp partials ----
+    if (kind == kArgmax) {
+      warp_argmax(mt, idx);
+      const int bad = __any_sync(kFull, (mxt != mxt) || mxt == INFINITY);
+      if (lane == 0) {
+        sm.wpart[cw] = make_float4(mt, 0.0f, 0.0f, 0.0f);
+        sm.widx[cw] = idx;
+        sm.wbad[cw] = bad;
+      }
+    } else {
+      float s0, s1;
+      upk(st, s0, s1);
+      float sT = s0 + s1;
+      upk(sd, s0, s1);
+      float sD = s0 + s1;
+      const float Mwt = warp_max(mt), Mwd = warp_max(md);
+      sT = (sT > 0.0f) ? sT * ex2((mt - Mwt) * k) : 0.0f;
+      sD = (sD > 0.0f) ? sD * ex2((md - Mwd) * k) : 0.0f;
+      sT = warp_sum_lane0(sT);
+      sD = warp_sum_lane0(sD);
+      const float mxa = max_nan(mxt, mxd);
+      const int bad = __any_sync(kFull, (mxa != mxa) || mxa == INFINITY);
+      if (lane == 0) {
+        sm.wpart[cw] = make_float4(Mwt, sT, Mwd, sD);
+        sm.wbad[cw] = bad;
+      }
+    }
+    named_bar_sync(kConsumerBar, kCT);
+
+    // ---- the cluster exchange: this position's softmax partials + the pending residual totals ----
+    exchange(true, kind, p, x, k, zx_t, zx_d, u_acc, u_res, u_bon);
     if (sm.stop_snap) break;
+    finish_pending();
 
     if (kind == kArgmax) {
       if (rank == 0 && cw == 0) {
@@ -577,12 +741,30 @@ __global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P)
     }
 
     const float kk = sm.k, ct = sm.ct, cd = sm.cd, cb = sm.cb;
-    const int pbad = sm.bad;
-    float alpha = 0.0f;
+    const int cbad = sm.bad;
 
-    if (kind == kVerify) {
-      // ---- pass 2: residual weights of the chunk, re-read from L2; one sum per vector ----
-      float W = 0.0f;
+    if (kind == kBonus) {
+      // Bonus token from p at position gamma_b ([R] One round, step 5).
+      const int dch = cbad ? -1 : sm.draw_chunk;
+      const float tl = sm.t_local;
+      if (dch < 0) {
+        if (rank == 0 && cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagBad, 0.0f, 0.0f, 0.0f, lane);
+      } else if (rank == dch) {
+        fill_p_sums(rowt, kk, cb);
+        named_bar_sync(kConsumerBar, kCT);
+        int finisher = 0;
+        const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm, ctid,
+                                         finisher);
+        if (cw == finisher)
+          finish_position(P, p.b, p.i, p.gb, tok, (tok < 0 ? kFlagBad : 0) | kFlagAccept, 0.0f, 0.0f,
+                          0.0f, lane);
+      }
+      continue;
+    }
+
+    // ---- drafted position: pass 2, the residual weights of the chunk re-read from L2 ----
+    float W = 0.0f;
+    if (!cbad) {
       const f32x2 k2 = pk(kk, kk), c2 = pk(ct, cd);
       const uint4* vt = reinterpret_cast<const uint4*>(rowt);
       const uint4* vd = reinterpret_cast<const uint4*>(rowd);
@@ -606,88 +788,32 @@ __global__ void __launch_bounds__(kThreadsS, 2) sv_stream_kernel(const Params P)
         usum[u - u0] = sv;
         W += sv;
       }
-      const float ws = warp_sum_lane0(W);
-      if (lane == 0) sm.wsum2[cw] = ws;
-      named_bar_sync(kConsumerBar, kCT);
-
-      // ---- exchange 2: residual chunk totals ----
-      const uint32_t par2 = e2 & 1, ph2 = (e2 >> 1) & 1;
-      ++e2;
-      if (cw == 0) {
-        const float wc = warp_sum_lane0(lane < kCW ? sm.wsum2[lane] : 0.0f);
-        if (lane < C) {
-          st_cluster_f32(map_to_rank(smem_addr(&sm.xch2[par2][rank]), lane), wc);
-          mbar_arrive_remote(map_to_rank(smem_addr(&sm.xbar2[par2]), lane));
-        }
-        const bool arrived = mbar_wait_cluster(smem_addr(&sm.xbar2[par2]), ph2);
-        if (!arrived) set_status(P, sm, kStatusTimeout);
-        const float w_r = lane < C ? sm.xch2[par2][lane] : 0.0f;
-        const float incl_w = warp_incl_scan(w_r, lane);
-        const float Wt = __shfl_sync(kFull, incl_w, 31);
-        float excl_w = __shfl_up_sync(kFull, incl_w, 1);
-        if (lane == 0) excl_w = 0.0f;
-        // Replacement from max(0, p - q) / sum max(0, p - q) ([R] One round, step 4): the chunk
-        // whose inclusive prefix first exceeds u * W (else, by rounding, the last positive chunk).
-        const float t = u_res * Wt;
-        const unsigned hit = __ballot_sync(kFull, lane < C && w_r > 0.0f && incl_w > t);
-        const unsigned pos = __ballot_sync(kFull, lane < C && w_r > 0.0f);
-        const int c = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
-        const float tl = t - __shfl_sync(kFull, excl_w, c);
-        if (lane == 0) {
-          sm.alpha = fminf(1.0f, fmaxf(0.0f, 1.0f - Wt));
-          if (sm.acc) {
-            sm.draw_chunk = -1;
-          } else if (Wt > 0.0f) {
-            sm.draw_chunk = c;
-            sm.t_local = tl;
-            sm.draw_resid = 1;
-          } else {                                   // zero residual mass: draw from p
-            sm.draw_chunk = sm.p_chunk;
-            sm.t_local = sm.p_tlocal;
-            sm.draw_resid = 0;
-          }
-          sm.stop_snap = sm.stop;
-        }
-      }
-      named_bar_sync(kConsumerBar, kCT);
-      if (sm.stop_snap) break;
-      alpha = sm.alpha;
     }
-
-    // ---- the draw and the position's finish ----
-    const int dchunk = sm.draw_chunk;
-    if (pbad || dchunk < 0) {
-      if (rank == 0 && cw == 0)
-        finish_position(P, p.b, p.i, p.gb, -1, pbad ? kFlagBad : kFlagAccept, alpha, sm.px, sm.qx,
-                        lane);
-      continue;
-    }
-    if (rank == dchunk) {
-      const bool resid = sm.draw_resid != 0;
-      const float tl = sm.t_local, px = sm.px, qx = sm.qx;
-      const int acc = sm.acc;
-      if (!resid) {
-        // Per-vector sums of p's weights exp2(z k + cb), re-read from L2.
-        const uint4* vt = reinterpret_cast<const uint4*>(rowt);
-        int u = u0 + ctid;
-        for (; u + 3 * kCT < u1; u += 4 * kCT) {
-          uint4 t[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) t[j] = ld_stream_v4(vt + u + j * kCT);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) usum[u + j * kCT - u0] = p_vec_sum<BF16>(t[j], kk, cb);
-        }
-        for (; u < u1; u += kCT) usum[u - u0] = p_vec_sum<BF16>(ld_stream_v4(vt + u), kk, cb);
-        named_bar_sync(kConsumerBar, kCT);
-      }
-      int finisher = 0;
-      const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, resid, kk, ct, cd, cb, sm, ctid,
-                                       finisher);
-      if (cw == finisher) {
-        const int flags = (tok < 0 ? kFlagBad : 0) | ((kind == kBonus || acc) ? kFlagAccept : 0);
-        finish_position(P, p.b, p.i, p.gb, tok, flags, alpha, px, qx, lane);
-      }
-    }
+    const float ws = warp_sum_lane0(W);
+    if (lane == 0) sm.wsum2[cw] = ws;
+    // The position becomes pending: its residual totals ride on the next exchange.
+    pv = true;
+    pb = p.b;
+    pi = p.i;
+    pgb = p.gb;
+    pacc = sm.acc;
+    pbad = cbad;
+    prt = rowt;
+    prd = rowd;
+    pkk = kk;
+    pct = ct;
+    pcd = cd;
+    pcb = cb;
+    ppx = sm.px;
+    pqx = sm.qx;
+    pp_chunk = sm.p_chunk;
+    pp_tlocal = sm.p_tlocal;
+    pu_res = u_res;
+  }
+  if (pv && !sm.stop_snap) {
+    named_bar_sync(kConsumerBar, kCT);   // the last residual partials are in place
+    exchange(false, kVerify, Pos{}, -1, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
+    finish_pending();
   }
 
   // ---- no CTA leaves while a peer may still write into its shared memory ----
@@ -704,6 +830,10 @@ const void* stream_fn(bool bf16) {
 
 cudaError_t stream_attrs(const void* fn, int C) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBytes);
+  if (e != cudaSuccess) return e;
+  // Two CTAs per SM need the largest shared-memory carveout.
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   if (C > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
