@@ -27,7 +27,7 @@ constexpr int kMaxCluster = 16;
 constexpr int kStreamMaxUnits = 4864;
 
 enum : int { kVerify = 0, kBonus = 1, kArgmax = 2 };
-enum : int { kFlagAccept = 1, kFlagBad = 2 };
+enum : int { kFlagAccept = 1, kFlagBad = 2, kFlagDone = 4 };
 
 struct Params {
   const void* zt;            // [B, G+1, V] target logits
@@ -389,7 +389,7 @@ __device__ __forceinline__ void finish_position(const Params& P, int b, int i, i
   unsigned old = 0;
   __syncwarp();
   if (lane == 0) {
-    P.rec[(size_t)b * G1 + i] = make_int2(cand, flags);
+    P.rec[(size_t)b * G1 + i] = make_int2(cand, flags | kFlagDone);
     __threadfence();
     old = atomicAdd(P.cnt + b, 1u);
   }
@@ -428,6 +428,19 @@ __device__ __forceinline__ void finish_position(const Params& P, int b, int i, i
     P.out_num[b] = err ? -1 : kk + 1;
     P.cnt[b] = 0u;                                     // leave the workspace zeroed
   }
+}
+
+// Whether a position of row b before position i has already recorded a rejection (visible to this
+// thread now; one full warp, every lane gets the answer). A rejected or bonus position after such
+// a rejection is never emitted, so its draw can be skipped. Records not yet visible read as
+// "no rejection", which only means the draw is done.
+__device__ __forceinline__ bool earlier_rejection(const Params& P, int b, int i, int lane) {
+  bool rej = false;
+  for (int j = lane; j < i; j += 32) {
+    const int f = __ldcg(&P.rec[(size_t)b * (P.G + 1) + j].y);
+    rej |= (f & kFlagDone) && !(f & kFlagAccept);
+  }
+  return __any_sync(kFull, rej);
 }
 
 // ------------------------------------------------------------------------------------------------

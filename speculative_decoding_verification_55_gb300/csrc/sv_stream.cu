@@ -67,7 +67,9 @@ constexpr int kSlotUnits = kSlotBytes / 16;
 constexpr int kNumSlots = SV_STREAM_RING_SLOTS;
 static_assert(kSlotUnits % kCT == 0, "a ring slot splits evenly over the consumer threads");
 constexpr int kRingBytes = kSlotBytes * kNumSlots;
-constexpr int kDynBytes = kRingBytes + kStreamMaxUnits * 4;   // ring + per-vector sums
+// Per-batch reference maxima of a bonus position's pass 1: one per (ring slot, consumer thread).
+constexpr int kMaxBatches = (kStreamMaxUnits / kSlotUnits + 1) * kCT;
+constexpr int kDynBytes = kRingBytes + kStreamMaxUnits * 4 + kMaxBatches * 4;  // ring, sums, maxima
 constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
 
 enum : unsigned { kStatusTimeout = 1u };
@@ -97,6 +99,14 @@ struct Shared {
   // the draw's crossing vector, handed from the thread that found it to the finishing warp
   int dj, dover;
   float dbefore;
+  int skip;                          // the drawing CTA saw an earlier rejection in the row
+  // the pending drafted position (kept here, not in registers, to leave room for the hot loops)
+  struct {
+    const char* rt;
+    const char* rd;
+    int b, i, gb, acc, bad, p_chunk;
+    float k, ct, cd, cb, px, qx, p_tlocal, u_res;
+  } pend;
 };
 
 struct Pos {
@@ -204,6 +214,51 @@ __device__ __forceinline__ void online_update_batch(const uint4 (&v)[N], float k
     }
   }
   s = add2(s, s2);
+}
+
+// online_update_batch that also keeps, for a bonus position's later draw, each vector's sum of
+// exp2((z - m) k) in vsum[j] (m = the running max after this batch, returned in `ref`).
+template <bool BF16, int N>
+__device__ __forceinline__ void online_update_batch_keep(const uint4 (&v)[N], float k, float& m,
+                                                         f32x2& s, float& mx, float (&vsum)[N]) {
+  float vm = -INFINITY;
+  if (BF16) {
+    uint32_t a = bmax2_nan(bmax2_nan(v[0].x, v[0].y), bmax2_nan(v[0].z, v[0].w));
+#pragma unroll
+    for (int j = 1; j < N; ++j)
+      a = bmax2_nan(a, bmax2_nan(bmax2_nan(v[j].x, v[j].y), bmax2_nan(v[j].z, v[j].w)));
+    vm = max_nan(bf_lo(a), bf_hi(a));
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; ++j) vm = max_nan(vm, vec_max<false>(v[j]));
+  }
+  mx = max_nan(mx, vm);
+  if (vm > m) {
+    float s0, s1;
+    upk(s, s0, s1);
+    const float f = ex2((m - vm) * k);
+    s = pk(s0 * f, s1 * f);
+    m = vm;
+  }
+  const float c = -m * k;
+  const f32x2 k2 = pk(k, k), c2 = pk(c, c);
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    f32x2 u2 = pk(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float a0, a1;
+      if (BF16) upk(fma2(pk(bf_lo(w[q]), bf_hi(w[q])), k2, c2), a0, a1);
+      else if (q < 2) upk(fma2(pk(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1])), k2, c2), a0, a1);
+      else break;
+      u2 = add2(u2, pk(ex2(a0), ex2(a1)));
+    }
+    float u0, u1;
+    upk(u2, u0, u1);
+    vsum[j] = u0 + u1;
+    s = add2(s, u2);
+  }
 }
 
 // Pass-1 greedy update: running max and the lowest index holding it.
@@ -389,6 +444,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
   const int nsl = (cu + kSlotUnits - 1) / kSlotUnits;
   const size_t Vs = static_cast<size_t>(P.V);
   float* usum = reinterpret_cast<float*>(dyn + kRingBytes);
+  float* bref = usum + kStreamMaxUnits;
 
   if (tid == 0) {
     for (int s = 0; s < kNumSlots; ++s) {
@@ -449,25 +505,18 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
 
   // The pending drafted position: pass 2 done, its residual chunk totals ride on the next exchange,
   // after which its draw (if rejected) and finish happen. Uniform across the cluster.
-  bool pv = false;
-  int pb = 0, pi = 0, pgb = 0, pacc = 1, pbad = 0;
-  const char* prt = nullptr;
-  const char* prd = nullptr;
-  float pkk = 0.0f, pct = 0.0f, pcd = 0.0f, pcb = 0.0f, ppx = 0.0f, pqx = 0.0f;
-  int pp_chunk = 0;                          // pending: chunk of the fallback draw from p
-  float pp_tlocal = 0.0f;
-  float pu_res = 0.0f;                       // consumer warp 0: the pending residual uniform
+  bool pv = false;                 // a pending position exists (its fields are in sm.pend)
 
   // Per-vector sums of p's unnormalised weights exp2(z k + cb) of this CTA's chunk, from L2.
   auto fill_p_sums = [&](const char* rt, float kk, float cbv) {
     const uint4* vt = reinterpret_cast<const uint4*>(rt);
     int u = u0 + ctid;
-    for (; u + 3 * kCT < u1; u += 4 * kCT) {
-      uint4 t[4];
+    for (; u + 7 * kCT < u1; u += 8 * kCT) {
+      uint4 t[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) t[j] = ld_stream_v4(vt + u + j * kCT);
+      for (int j = 0; j < 8; ++j) t[j] = ld_stream_v4(vt + u + j * kCT);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) usum[u + j * kCT - u0] = p_vec_sum<BF16>(t[j], kk, cbv);
+      for (int j = 0; j < 8; ++j) usum[u + j * kCT - u0] = p_vec_sum<BF16>(t[j], kk, cbv);
     }
     for (; u < u1; u += kCT) usum[u - u0] = p_vec_sum<BF16>(ld_stream_v4(vt + u), kk, cbv);
   };
@@ -582,14 +631,14 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
         const float Wt = __shfl_sync(kFull, incl_w, 31);
         float excl_w = __shfl_up_sync(kFull, incl_w, 1);
         if (lane == 0) excl_w = 0.0f;
-        const float t = pu_res * Wt;
+        const float t = sm.pend.u_res * Wt;
         const unsigned hit = __ballot_sync(kFull, lane < C && w_r > 0.0f && incl_w > t);
         const unsigned pos = __ballot_sync(kFull, lane < C && w_r > 0.0f);
         const int c = hit ? (__ffs(hit) - 1) : (pos ? (31 - __clz(pos)) : 0);
         const float tl = t - __shfl_sync(kFull, excl_w, c);
         if (lane == 0) {
           sm.pend_alpha = fminf(1.0f, fmaxf(0.0f, 1.0f - Wt));
-          sm.pend_chunk = (pacc || pbad) ? -1 : (Wt > 0.0f ? c : -2);
+          sm.pend_chunk = (sm.pend.acc || sm.pend.bad) ? -1 : (Wt > 0.0f ? c : -2);
           sm.pend_tlocal = tl;
           sm.pend_resid = Wt > 0.0f;
         }
@@ -607,17 +656,32 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     const float alpha = sm.pend_alpha;
     bool resid = sm.pend_resid != 0;
     float tl = sm.pend_tlocal;
+    const int pb = sm.pend.b, pi = sm.pend.i, pgb = sm.pend.gb;
+    const float ppx = sm.pend.px, pqx = sm.pend.qx;
     if (dch == -2) {                 // zero residual mass: draw from p with the residual uniform
-      dch = pp_chunk;
-      tl = pp_tlocal;
+      dch = sm.pend.p_chunk;
+      tl = sm.pend.p_tlocal;
       resid = false;
     }
     if (dch < 0) {
       if (rank == 0 && cw == 0)
-        finish_position(P, pb, pi, pgb, -1, pbad ? kFlagBad : kFlagAccept, alpha, ppx, pqx, lane);
+        finish_position(P, pb, pi, pgb, -1, sm.pend.bad ? kFlagBad : kFlagAccept, alpha, ppx, pqx,
+                        lane);
       return;
     }
     if (rank != dch) return;
+    if (cw == 0) {
+      const bool early = earlier_rejection(P, pb, pi, lane);
+      if (lane == 0) sm.skip = early;
+    }
+    named_bar_sync(kConsumerBar, kCT);
+    if (sm.skip) {                   // a rejection earlier in the row: this draw is never emitted
+      if (cw == 0) finish_position(P, pb, pi, pgb, -1, 0, alpha, ppx, pqx, lane);
+      return;
+    }
+    const char* prt = sm.pend.rt;
+    const char* prd = sm.pend.rd;
+    const float pkk = sm.pend.k, pct = sm.pend.ct, pcd = sm.pend.cd, pcb = sm.pend.cb;
     if (!resid) {
       fill_p_sums(prt, pkk, pcb);
       named_bar_sync(kConsumerBar, kCT);
@@ -656,6 +720,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     }
 
     // ---- pass 1 out of the ring ----
+    const bool kept = kind == kBonus && !pv;   // pass 1 keeps the bonus draw's vector sums
     const float k = p.greedy ? 0.0f : kLog2e / p.T;
     float mt = -INFINITY, md = -INFINITY, mxt = -INFINITY, mxd = -INFINITY;
     f32x2 st = pk(0.0f, 0.0f), sd = pk(0.0f, 0.0f);
@@ -680,6 +745,14 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
 #pragma unroll
             for (int j = 0; j < N; ++j)
               argmax_update<BF16>(v[j], (u0 + ks * kSlotUnits + ctid + j * kCT) * E, mt, idx, mxt);
+          } else if (row == 0 && kind == kBonus && !pv) {
+            // Keep each vector's p sum and the batch's reference max for the bonus draw.
+            float vs[N];
+            online_update_batch_keep<BF16, N>(v, k, mt, st, mxt, vs);
+#pragma unroll
+            for (int j = 0; j < N; ++j)
+              if (ctid + j * kCT < nu) usum[ks * kSlotUnits + ctid + j * kCT] = vs[j];
+            bref[ks * kCT + ctid] = mt;
           } else if (row == 0) {
             online_update_batch<BF16, N>(v, k, mt, st, mxt);
           } else {
@@ -750,7 +823,26 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       if (dch < 0) {
         if (rank == 0 && cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagBad, 0.0f, 0.0f, 0.0f, lane);
       } else if (rank == dch) {
-        fill_p_sums(rowt, kk, cb);
+        if (cw == 0) {
+          const bool early = earlier_rejection(P, p.b, p.i, lane);
+          if (lane == 0) sm.skip = early;
+        }
+        named_bar_sync(kConsumerBar, kCT);
+        if (sm.skip) {               // a rejection earlier in the row: the bonus is never emitted
+          if (cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagAccept, 0.0f, 0.0f, 0.0f, lane);
+          continue;
+        }
+        if (kept) {
+          // Rescale this thread's vector sums from pass 1 (kept against the batch's running max)
+          // to the global max: weight exp2(z k + cb), cb = -M k.
+          for (int ks = 0; ks < nsl; ++ks) {
+            const float f = ex2(fmaf(bref[ks * kCT + ctid], kk, cb));
+            const int nu = min(kSlotUnits, cu - ks * kSlotUnits);
+            for (int uu = ctid; uu < nu; uu += kCT) usum[ks * kSlotUnits + uu] *= f;
+          }
+        } else {
+          fill_p_sums(rowt, kk, cb);
+        }
         named_bar_sync(kConsumerBar, kCT);
         int finisher = 0;
         const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm, ctid,
@@ -791,24 +883,27 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     }
     const float ws = warp_sum_lane0(W);
     if (lane == 0) sm.wsum2[cw] = ws;
-    // The position becomes pending: its residual totals ride on the next exchange.
+    // The position becomes pending: its residual totals ride on the next exchange. Consumer
+    // thread 0 records it (every consumer reads it only after the next exchange's barrier).
     pv = true;
-    pb = p.b;
-    pi = p.i;
-    pgb = p.gb;
-    pacc = sm.acc;
-    pbad = cbad;
-    prt = rowt;
-    prd = rowd;
-    pkk = kk;
-    pct = ct;
-    pcd = cd;
-    pcb = cb;
-    ppx = sm.px;
-    pqx = sm.qx;
-    pp_chunk = sm.p_chunk;
-    pp_tlocal = sm.p_tlocal;
-    pu_res = u_res;
+    if (ctid == 0) {
+      sm.pend.b = p.b;
+      sm.pend.i = p.i;
+      sm.pend.gb = p.gb;
+      sm.pend.acc = sm.acc;
+      sm.pend.bad = cbad;
+      sm.pend.rt = rowt;
+      sm.pend.rd = rowd;
+      sm.pend.k = kk;
+      sm.pend.ct = ct;
+      sm.pend.cd = cd;
+      sm.pend.cb = cb;
+      sm.pend.px = sm.px;
+      sm.pend.qx = sm.qx;
+      sm.pend.p_chunk = sm.p_chunk;
+      sm.pend.p_tlocal = sm.p_tlocal;
+      sm.pend.u_res = u_res;
+    }
   }
   if (pv && !sm.stop_snap) {
     named_bar_sync(kConsumerBar, kCT);   // the last residual partials are in place
