@@ -62,7 +62,10 @@ namespace {
 constexpr int kCW = SV_STREAM_CONSUMER_WARPS;   // consumer warps
 constexpr int kCT = kCW * 32;                 // consumer threads
 constexpr int kThreadsS = kCT + 32;           // plus the producer warp
-constexpr int kSlotBytes = 16384;
+#ifndef SV_STREAM_SLOT_BYTES
+#define SV_STREAM_SLOT_BYTES 16384
+#endif
+constexpr int kSlotBytes = SV_STREAM_SLOT_BYTES;
 constexpr int kSlotUnits = kSlotBytes / 16;
 constexpr int kNumSlots = SV_STREAM_RING_SLOTS;
 static_assert(kSlotUnits % kCT == 0, "a ring slot splits evenly over the consumer threads");
@@ -104,7 +107,7 @@ struct Shared {
   struct {
     const char* rt;
     const char* rd;
-    int b, i, gb, acc, bad, p_chunk;
+    int b, i, gb, acc, bad, p_chunk, fin;
     float k, ct, cd, cb, px, qx, p_tlocal, u_res;
   } pend;
 };
@@ -194,26 +197,23 @@ __device__ __forceinline__ void online_update_batch(const uint4 (&v)[N], float k
   }
   const float c = -m * k;
   const f32x2 k2 = pk(k, k), c2 = pk(c, c);
-  f32x2 s2 = pk(0.0f, 0.0f);
+  f32x2 acc[4] = {pk(0.0f, 0.0f), pk(0.0f, 0.0f), pk(0.0f, 0.0f), pk(0.0f, 0.0f)};
 #pragma unroll
   for (int j = 0; j < N; ++j) {
     const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-    for (int q = 0; q < 4; q += 2) {
-      float a0, a1, b0, b1;
+    for (int q = 0; q < 4; ++q) {
+      float a0, a1;
       if (BF16) {
         upk(fma2(pk(bf_lo(w[q]), bf_hi(w[q])), k2, c2), a0, a1);
-        upk(fma2(pk(bf_lo(w[q + 1]), bf_hi(w[q + 1])), k2, c2), b0, b1);
-        s = add2(s, pk(ex2(a0), ex2(a1)));
-        s2 = add2(s2, pk(ex2(b0), ex2(b1)));
       } else {
-        upk(fma2(pk(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), k2, c2), a0, a1);
-        if (q == 0) s = add2(s, pk(ex2(a0), ex2(a1)));
-        else s2 = add2(s2, pk(ex2(a0), ex2(a1)));
+        if (q >= 2) break;
+        upk(fma2(pk(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1])), k2, c2), a0, a1);
       }
+      acc[(j * 4 + q) & 3] = add2(acc[(j * 4 + q) & 3], pk(ex2(a0), ex2(a1)));
     }
   }
-  s = add2(s, s2);
+  s = add2(s, add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
 }
 
 // online_update_batch that also keeps, for a bonus position's later draw, each vector's sum of
@@ -292,15 +292,15 @@ __device__ __forceinline__ void resid_pair(const uint4& t, const uint4& d, int e
 template <bool BF16>
 __device__ __forceinline__ float resid_vec_sum(const uint4& t, const uint4& d, f32x2 k2, f32x2 c2) {
   constexpr int E = BF16 ? 8 : 4;
-  float s = 0.0f;
+  float w[E];
 #pragma unroll
-  for (int e = 0; e < E; e += 2) {
-    float w0, w1;
-    resid_pair<BF16>(t, d, e, k2, c2, w0, w1);
-    s += w0;
-    s += w1;
+  for (int e = 0; e < E; e += 2) resid_pair<BF16>(t, d, e, k2, c2, w[e], w[e + 1]);
+#pragma unroll
+  for (int h = 1; h < E; h *= 2) {
+#pragma unroll
+    for (int e = 0; e < E; e += 2 * h) w[e] += w[e + h];
   }
-  return s;
+  return w[0];
 }
 
 // Sum of the unnormalised p weights exp2(z k + cb) of one vector.
@@ -466,6 +466,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     if (lane != 0) return;
     uint32_t tc = 0;
     bool ok = true;
+    const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
     for (int s = cid; s < total && ok; s += P.nclusters) {
       const Pos p = classify(P, s);
       if (!p.load) continue;
@@ -482,8 +483,9 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
           }
           const uint32_t bytes = static_cast<uint32_t>(min(kSlotUnits, cu - ks * kSlotUnits)) * 16;
           mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), bytes);
+          // A drafted position's chunks are read again by the residual pass: keep them in L2.
           bulk_g2s(ring_addr + slot * kSlotBytes, g + static_cast<size_t>(ks) * kSlotBytes, bytes,
-                   smem_addr(&sm.full[slot]));
+                   smem_addr(&sm.full[slot]), p.two ? keep : once);
         }
       }
     }
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       resid = false;
     }
     if (dch < 0) {
-      if (rank == 0 && cw == 0)
+      if (rank == sm.pend.fin && cw == 0)
         finish_position(P, pb, pi, pgb, -1, sm.pend.bad ? kFlagBad : kFlagAccept, alpha, ppx, pqx,
                         lane);
       return;
@@ -802,9 +804,12 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     exchange(true, kind, p, x, k, zx_t, zx_d, u_acc, u_res, u_bon);
     if (sm.stop_snap) break;
     finish_pending();
+    // The CTA that finishes this position when no draw picks one: rotates over the ranks so that
+    // the finishing work (records, counters, row emits) does not slow one rank down.
+    const int fin = static_cast<int>((ex - 1) % static_cast<uint32_t>(C));
 
     if (kind == kArgmax) {
-      if (rank == 0 && cw == 0) {
+      if (rank == fin && cw == 0) {
         const int acc = sm.acc;
         const int flags = (sm.bad ? kFlagBad : 0) | (acc ? kFlagAccept : 0);
         const float a = acc ? 1.0f : 0.0f;
@@ -821,7 +826,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       const int dch = cbad ? -1 : sm.draw_chunk;
       const float tl = sm.t_local;
       if (dch < 0) {
-        if (rank == 0 && cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagBad, 0.0f, 0.0f, 0.0f, lane);
+        if (rank == fin && cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagBad, 0.0f, 0.0f, 0.0f, lane);
       } else if (rank == dch) {
         if (cw == 0) {
           const bool early = earlier_rejection(P, p.b, p.i, lane);
@@ -857,6 +862,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     // ---- drafted position: pass 2, the residual weights of the chunk re-read from L2 ----
     float W = 0.0f;
     if (!cbad) {
+      const uint64_t last_use = l2_policy_evict_first();
       const f32x2 k2 = pk(kk, kk), c2 = pk(ct, cd);
       const uint4* vt = reinterpret_cast<const uint4*>(rowt);
       const uint4* vd = reinterpret_cast<const uint4*>(rowd);
@@ -865,8 +871,8 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
         uint4 t[4], d[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          t[j] = ld_stream_v4(vt + u + j * kCT);
-          d[j] = ld_stream_v4(vd + u + j * kCT);
+          t[j] = ld_stream_v4_hint(vt + u + j * kCT, last_use);
+          d[j] = ld_stream_v4_hint(vd + u + j * kCT, last_use);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -876,7 +882,8 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
         }
       }
       for (; u < u1; u += kCT) {
-        const float sv = resid_vec_sum<BF16>(ld_stream_v4(vt + u), ld_stream_v4(vd + u), k2, c2);
+        const float sv = resid_vec_sum<BF16>(ld_stream_v4_hint(vt + u, last_use),
+                                             ld_stream_v4_hint(vd + u, last_use), k2, c2);
         usum[u - u0] = sv;
         W += sv;
       }
@@ -903,6 +910,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       sm.pend.p_chunk = sm.p_chunk;
       sm.pend.p_tlocal = sm.p_tlocal;
       sm.pend.u_res = u_res;
+      sm.pend.fin = fin;
     }
   }
   if (pv && !sm.stop_snap) {
