@@ -69,6 +69,9 @@ constexpr int kSlotBytes = SV_STREAM_SLOT_BYTES;
 constexpr int kSlotUnits = kSlotBytes / 16;
 constexpr int kNumSlots = SV_STREAM_RING_SLOTS;
 static_assert(kSlotUnits % kCT == 0, "a ring slot splits evenly over the consumer threads");
+// A residual-pass slot holds kHalfUnits target vectors and the matching kHalfUnits draft vectors.
+constexpr int kHalfUnits = kSlotUnits / 2;
+static_assert(kHalfUnits % kCT == 0, "a residual slot splits evenly over the consumer threads");
 constexpr int kRingBytes = kSlotBytes * kNumSlots;
 // Per-batch reference maxima of a bonus position's pass 1: one per (ring slot, consumer thread).
 constexpr int kMaxBatches = (kStreamMaxUnits / kSlotUnits + 1) * kCT;
@@ -441,7 +444,8 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
   const int u0 = min(rank * P.per, P.units);
   const int u1 = min(u0 + P.per, P.units);
   const int cu = u1 - u0;
-  const int nsl = (cu + kSlotUnits - 1) / kSlotUnits;
+  const int nsl = (cu + kSlotUnits - 1) / kSlotUnits;      // pass-1 slots per row
+  const int nsl2 = (cu + kHalfUnits - 1) / kHalfUnits;     // residual-pass slots per position
   const size_t Vs = static_cast<size_t>(P.V);
   float* usum = reinterpret_cast<float*>(dyn + kRingBytes);
   float* bref = usum + kStreamMaxUnits;
@@ -487,6 +491,25 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
           bulk_g2s(ring_addr + slot * kSlotBytes, g + static_cast<size_t>(ks) * kSlotBytes, bytes,
                    smem_addr(&sm.full[slot]), p.two ? keep : once);
         }
+      }
+      if (!p.two || !ok) continue;
+      // Residual pass of a drafted position: the same chunk again, now from L2, each slot holding
+      // kHalfUnits target vectors and the matching draft vectors. These copies depend on nothing
+      // the exchange produces, so they land while the consumers wait for it.
+      const char* gt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES + (size_t)u0 * 16;
+      const char* gd = static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES + (size_t)u0 * 16;
+      for (int ks = 0; ks < nsl2; ++ks, ++tc) {
+        const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
+        if (!mbar_wait(smem_addr(&sm.empty[slot]), par ^ 1) || sm.stop) {
+          ok = false;
+          break;
+        }
+        const uint32_t bytes = static_cast<uint32_t>(min(kHalfUnits, cu - ks * kHalfUnits)) * 16;
+        const size_t off = static_cast<size_t>(ks) * kHalfUnits * 16;
+        mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), 2 * bytes);
+        bulk_g2s(ring_addr + slot * kSlotBytes, gt + off, bytes, smem_addr(&sm.full[slot]), once);
+        bulk_g2s(ring_addr + slot * kSlotBytes + kSlotBytes / 2, gd + off, bytes,
+                 smem_addr(&sm.full[slot]), once);
       }
     }
     if (!ok) {
@@ -767,6 +790,14 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     }
     if (timed_out) set_status(P, sm, kStatusTimeout);
     if (!ok) {                       // drafted token or uniform out of range: the row is an error
+      if (p.two) {                   // the producer also streamed the residual-pass slots: drain
+        for (int ks = 0; ks < nsl2; ++ks, ++tc) {
+          const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
+          if (!mbar_wait(smem_addr(&sm.full[slot]), par)) set_status(P, sm, kStatusTimeout);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
+        }
+      }
       if (p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
       continue;
     }
@@ -859,34 +890,28 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       continue;
     }
 
-    // ---- drafted position: pass 2, the residual weights of the chunk re-read from L2 ----
+    // ---- drafted position: pass 2, the residual weights of the chunk, out of the ring ----
     float W = 0.0f;
-    if (!cbad) {
-      const uint64_t last_use = l2_policy_evict_first();
+    {
       const f32x2 k2 = pk(kk, kk), c2 = pk(ct, cd);
-      const uint4* vt = reinterpret_cast<const uint4*>(rowt);
-      const uint4* vd = reinterpret_cast<const uint4*>(rowd);
-      int u = u0 + ctid;
-      for (; u + 3 * kCT < u1; u += 4 * kCT) {
-        uint4 t[4], d[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          t[j] = ld_stream_v4_hint(vt + u + j * kCT, last_use);
-          d[j] = ld_stream_v4_hint(vd + u + j * kCT, last_use);
+      bool tmo = false;
+      for (int ks = 0; ks < nsl2; ++ks, ++tc) {
+        const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
+        if (!mbar_wait(smem_addr(&sm.full[slot]), par)) tmo = true;
+        const int nu = min(kHalfUnits, cu - ks * kHalfUnits);
+        const uint4* st4 = ringv + slot * kSlotUnits;
+        const uint4* sd4 = st4 + kHalfUnits;
+        if (!cbad && !tmo) {
+          for (int uu = ctid; uu < nu; uu += kCT) {
+            const float sv = resid_vec_sum<BF16>(st4[uu], sd4[uu], k2, c2);
+            usum[ks * kHalfUnits + uu] = sv;
+            W += sv;
+          }
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float sv = resid_vec_sum<BF16>(t[j], d[j], k2, c2);
-          usum[u + j * kCT - u0] = sv;
-          W += sv;
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[slot]));
       }
-      for (; u < u1; u += kCT) {
-        const float sv = resid_vec_sum<BF16>(ld_stream_v4_hint(vt + u, last_use),
-                                             ld_stream_v4_hint(vd + u, last_use), k2, c2);
-        usum[u - u0] = sv;
-        W += sv;
-      }
+      if (tmo) set_status(P, sm, kStatusTimeout);
     }
     const float ws = warp_sum_lane0(W);
     if (lane == 0) sm.wsum2[cw] = ws;
