@@ -261,6 +261,32 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Non-blocking test of a phase (for a thread that serves several barriers in turn).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// One poll that may suspend the thread for up to `ns` nanoseconds while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded waits: every spin gives up after kSpinLimit polls (each poll may suspend the thread for a
 // hardware-chosen time), so a broken protocol ends the kernel with an error status instead of a hang.
 constexpr int kSpinLimit = 1 << 22;
@@ -336,6 +362,37 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
     if (lane >= o) v += y;
   }
   return v;
+}
+
+// The same over the first n lanes only (n a power of two, 1 <= n <= 32): log2(n) shuffle stages
+// instead of five. Lanes below n get the result; the others hold partial values.
+__device__ __forceinline__ float lanes_max(float v, int n) {
+  for (int o = 1; o < n; o <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float lanes_sum(float v, int n) {
+  for (int o = 1; o < n; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float lanes_incl_scan(float v, int lane, int n) {
+  for (int o = 1; o < n; o <<= 1) {
+    const float y = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
+__device__ __forceinline__ void lanes_argmax(float& v, int& i, int n) {
+  for (int o = 1; o < n; o <<= 1) {
+    const float ov = __shfl_xor_sync(kFull, v, o);
+    const int oi = __shfl_xor_sync(kFull, i, o);
+    if (ov > v || (ov == v && oi < i)) {
+      v = ov;
+      i = oi;
+    }
+  }
 }
 
 // (value, index) argmax over the warp: larger value wins, equal values keep the lower index.

@@ -8,7 +8,7 @@
 // producer warp.
 //
 // Producer warp (one thread). Walks the cluster's positions and streams this CTA's chunks through a
-// ring of kNumSlots x 16 KB shared-memory slots with cp.async.bulk (the TMA engine), one full/empty
+// ring of kNumSlots x kSlotBytes shared-memory slots with cp.async.bulk (the TMA engine), one full/empty
 // mbarrier pair per slot. It runs ahead of the consumers by the ring's capacity, so HBM keeps
 // streaming while the consumers exchange partial results.
 //
@@ -25,15 +25,16 @@
 //   xchg     each CTA combines the C records in the same fixed order: global max M, normaliser S
 //            (an inclusive scan over ranks = the chunk-level CDF of p), the accept test
 //            u < min(1, p(x)/q(x)), the chunk that holds a bonus-draw threshold.
-//   pass 2   (drafted positions) the chunk again, now from L2 where pass 1 left it: residual
-//            weights max(0, p - q), p and q normalised inside the exponent; one sum per 16-byte
-//            vector is kept in shared memory for the draw. alpha = 1 - W with W the residual mass:
-//            sum min(p, q) + sum max(0, p - q) = sum p = 1 ([R] Why the output is exactly the
-//            target's).
+//   pass 2   (drafted positions) the chunk again, copied from L2 where pass 1 left it through
+//            the same ring (each slot half target vectors, half the matching draft vectors):
+//            residual weights max(0, p - q), p and q normalised inside the exponent; one sum per
+//            group of kGrp 16-byte vectors is kept in shared memory for the draw. alpha = 1 - W
+//            with W the residual mass: sum min(p, q) + sum max(0, p - q) = sum p = 1 ([R] Why the
+//            output is exactly the target's).
 //   next     the residual chunk totals (inclusive scan over ranks) arrive with the next exchange.
-//   draw     the CTA whose chunk holds the inverse-CDF threshold scans its per-vector sums in index
-//            order (block-wide prefix sum), reloads the one vector that crosses the threshold and
-//            picks the token inside it. A bonus draw first fills the per-vector sums of p from L2.
+//   draw     the CTA whose chunk holds the inverse-CDF threshold scans its group sums in index
+//            order (block-wide prefix sum), reloads the group that crosses the threshold and
+//            picks the token inside it. A bonus draw first fills the group sums of p from L2.
 //   finish   the CTA holding the position's final result writes it; the row's last position to
 //            finish writes the row's outputs (an arrival counter per row, no waiting).
 // Every wait is bounded; a wait that gives up sets the status word and ends the kernel.
@@ -48,13 +49,13 @@
 namespace sv {
 namespace {
 
-// Four CTAs per SM, each 4 consumer warps + 1 producer warp with a 2 x 16 KB ring: four
+// Four CTAs per SM, each 4 consumer warps + 1 producer warp with a 3 x 16 KB ring: four
 // independent position streams per SM, so one CTA's exchange waits overlap another's arithmetic.
 #ifndef SV_STREAM_CONSUMER_WARPS
 #define SV_STREAM_CONSUMER_WARPS 4
 #endif
 #ifndef SV_STREAM_RING_SLOTS
-#define SV_STREAM_RING_SLOTS 2
+#define SV_STREAM_RING_SLOTS 3
 #endif
 #ifndef SV_STREAM_CTAS_PER_SM
 #define SV_STREAM_CTAS_PER_SM 4
@@ -65,6 +66,10 @@ constexpr int kThreadsS = kCT + 32;           // plus the producer warp
 #ifndef SV_STREAM_SLOT_BYTES
 #define SV_STREAM_SLOT_BYTES 16384
 #endif
+// Consecutive 16-byte vectors summed into one entry of the draw's weight table.
+#ifndef SV_STREAM_GROUP
+#define SV_STREAM_GROUP 4
+#endif
 constexpr int kSlotBytes = SV_STREAM_SLOT_BYTES;
 constexpr int kSlotUnits = kSlotBytes / 16;
 constexpr int kNumSlots = SV_STREAM_RING_SLOTS;
@@ -73,9 +78,11 @@ static_assert(kSlotUnits % kCT == 0, "a ring slot splits evenly over the consume
 constexpr int kHalfUnits = kSlotUnits / 2;
 static_assert(kHalfUnits % kCT == 0, "a residual slot splits evenly over the consumer threads");
 constexpr int kRingBytes = kSlotBytes * kNumSlots;
-// Per-batch reference maxima of a bonus position's pass 1: one per (ring slot, consumer thread).
-constexpr int kMaxBatches = (kStreamMaxUnits / kSlotUnits + 1) * kCT;
-constexpr int kDynBytes = kRingBytes + kStreamMaxUnits * 4 + kMaxBatches * 4;  // ring, sums, maxima
+constexpr int kGrp = SV_STREAM_GROUP;
+static_assert(kGrp == 1 || kGrp == 2 || kGrp == 4 || kGrp == 8, "groups of lanes for a shuffle sum");
+static_assert(kHalfUnits % kGrp == 0, "a vector group never straddles two ring slots");
+constexpr int kMaxGroups = (kStreamMaxUnits + kGrp - 1) / kGrp;
+constexpr int kDynBytes = kRingBytes + kMaxGroups * 4;   // ring, the draw's group weights
 constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
 
 enum : unsigned { kStatusTimeout = 1u };
@@ -219,51 +226,6 @@ __device__ __forceinline__ void online_update_batch(const uint4 (&v)[N], float k
   s = add2(s, add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
 }
 
-// online_update_batch that also keeps, for a bonus position's later draw, each vector's sum of
-// exp2((z - m) k) in vsum[j] (m = the running max after this batch, returned in `ref`).
-template <bool BF16, int N>
-__device__ __forceinline__ void online_update_batch_keep(const uint4 (&v)[N], float k, float& m,
-                                                         f32x2& s, float& mx, float (&vsum)[N]) {
-  float vm = -INFINITY;
-  if (BF16) {
-    uint32_t a = bmax2_nan(bmax2_nan(v[0].x, v[0].y), bmax2_nan(v[0].z, v[0].w));
-#pragma unroll
-    for (int j = 1; j < N; ++j)
-      a = bmax2_nan(a, bmax2_nan(bmax2_nan(v[j].x, v[j].y), bmax2_nan(v[j].z, v[j].w)));
-    vm = max_nan(bf_lo(a), bf_hi(a));
-  } else {
-#pragma unroll
-    for (int j = 0; j < N; ++j) vm = max_nan(vm, vec_max<false>(v[j]));
-  }
-  mx = max_nan(mx, vm);
-  if (vm > m) {
-    float s0, s1;
-    upk(s, s0, s1);
-    const float f = ex2((m - vm) * k);
-    s = pk(s0 * f, s1 * f);
-    m = vm;
-  }
-  const float c = -m * k;
-  const f32x2 k2 = pk(k, k), c2 = pk(c, c);
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-    f32x2 u2 = pk(0.0f, 0.0f);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float a0, a1;
-      if (BF16) upk(fma2(pk(bf_lo(w[q]), bf_hi(w[q])), k2, c2), a0, a1);
-      else if (q < 2) upk(fma2(pk(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1])), k2, c2), a0, a1);
-      else break;
-      u2 = add2(u2, pk(ex2(a0), ex2(a1)));
-    }
-    float u0, u1;
-    upk(u2, u0, u1);
-    vsum[j] = u0 + u1;
-    s = add2(s, u2);
-  }
-}
-
 // Pass-1 greedy update: running max and the lowest index holding it.
 template <bool BF16>
 __device__ __forceinline__ void argmax_update(const uint4& v, int base, float& m, int& idx, float& mx) {
@@ -316,19 +278,28 @@ __device__ __forceinline__ float p_vec_sum(const uint4& t, float k, float cb) {
   return s;
 }
 
-// The draw inside this CTA's chunk. usum[j] holds the weight of vector u0 + j (residual or p
-// weights, per `resid`); the token is the first logit whose running weight exceeds t_local, else
-// (rounding) the last logit with positive weight. Block-wide prefix sum over the vector sums, then
-// one reload of the crossing vector. Returns the token in warp `finisher` (all its lanes); other
-// warps return -1. All consumer threads call it.
+// Sum over the kGrp consecutive lanes of a group (vectors u, u+1, ... of a chunk sit in
+// consecutive lanes); every lane of the group gets the total.
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < kGrp; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// The draw inside this CTA's chunk. usum[g] holds the weight of vectors u0 + g*kGrp ... +kGrp-1
+// (residual or p weights, per `resid`); the token is the first logit whose running weight exceeds
+// t_local, else (rounding) the last logit with positive weight. Block-wide prefix sum over the
+// group sums, then one reload of the crossing group. Returns the token in warp `finisher` (all its
+// lanes); other warps return -1. All consumer threads call it.
 template <bool BF16>
 __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, const char* rowt,
                           const char* rowd, bool resid, float k, float ct, float cd, float cb,
                           Shared& sm, int ctid, int& finisher) {
   constexpr int E = BF16 ? 8 : 4;
   const int lane = ctid & 31, cw = ctid >> 5;
-  const int run = (cu + kCT - 1) / kCT;
-  const int r0 = min(ctid * run, cu), r1 = min(r0 + run, cu);
+  const int cg = (cu + kGrp - 1) / kGrp;
+  const int run = (cg + kCT - 1) / kCT;
+  const int r0 = min(ctid * run, cg), r1 = min(r0 + run, cg);
   float tsum = 0.0f;
   int last_j = -1;
   for (int j = r0; j < r1; ++j) {
@@ -394,34 +365,38 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
   const bool overrun = sm.dover != 0;
   int tok = -1;
   if (lane == 0 && vj >= 0) {
-    const int u = u0 + vj;
-    const uint4 t = ld_stream_v4(reinterpret_cast<const uint4*>(rowt) + u);
-    const uint4 d = resid ? ld_stream_v4(reinterpret_cast<const uint4*>(rowd) + u) : t;
+    // Scan the group's vectors in index order: the first logit whose running weight exceeds the
+    // threshold, else the last positive one.
     const f32x2 k2 = pk(k, k), c2 = pk(ct, cd);
+    const int ga = u0 + vj * kGrp, gz = min(ga + kGrp, u0 + cu);
     float c = before;
     int pick = -1, lastp = -1;
+    for (int u = ga; u < gz && (pick < 0 || overrun); ++u) {
+      const uint4 t = ld_stream_v4(reinterpret_cast<const uint4*>(rowt) + u);
+      const uint4 d = resid ? ld_stream_v4(reinterpret_cast<const uint4*>(rowd) + u) : t;
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      float w0, w1;
-      if (resid) {
-        resid_pair<BF16>(t, d, e, k2, c2, w0, w1);
-      } else {
-        w0 = ex2(fmaf(vec_get<BF16>(t, e), k, cb));
-        w1 = ex2(fmaf(vec_get<BF16>(t, e + 1), k, cb));
-      }
-      if (w0 > 0.0f) {
-        lastp = e;
-        c += w0;
-        if (pick < 0 && c > t_local) pick = e;
-      }
-      if (w1 > 0.0f) {
-        lastp = e + 1;
-        c += w1;
-        if (pick < 0 && c > t_local) pick = e + 1;
+      for (int e = 0; e < E; e += 2) {
+        float w0, w1;
+        if (resid) {
+          resid_pair<BF16>(t, d, e, k2, c2, w0, w1);
+        } else {
+          w0 = ex2(fmaf(vec_get<BF16>(t, e), k, cb));
+          w1 = ex2(fmaf(vec_get<BF16>(t, e + 1), k, cb));
+        }
+        if (w0 > 0.0f) {
+          lastp = u * E + e;
+          c += w0;
+          if (pick < 0 && c > t_local) pick = u * E + e;
+        }
+        if (w1 > 0.0f) {
+          lastp = u * E + e + 1;
+          c += w1;
+          if (pick < 0 && c > t_local) pick = u * E + e + 1;
+        }
       }
     }
     if (pick < 0 || overrun) pick = lastp;
-    tok = pick >= 0 ? u * E + pick : -1;
+    tok = pick;
   }
   return __shfl_sync(kFull, tok, 0);
 }
@@ -447,8 +422,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
   const int nsl = (cu + kSlotUnits - 1) / kSlotUnits;      // pass-1 slots per row
   const int nsl2 = (cu + kHalfUnits - 1) / kHalfUnits;     // residual-pass slots per position
   const size_t Vs = static_cast<size_t>(P.V);
-  float* usum = reinterpret_cast<float*>(dyn + kRingBytes);
-  float* bref = usum + kStreamMaxUnits;
+  float* usum = reinterpret_cast<float*>(dyn + kRingBytes);   // the draw's group weights
 
   if (tid == 0) {
     for (int s = 0; s < kNumSlots; ++s) {
@@ -532,18 +506,25 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
   // after which its draw (if rejected) and finish happen. Uniform across the cluster.
   bool pv = false;                 // a pending position exists (its fields are in sm.pend)
 
-  // Per-vector sums of p's unnormalised weights exp2(z k + cb) of this CTA's chunk, from L2.
+  // Group sums of p's unnormalised weights exp2(z k + cb) over this CTA's chunk, from L2.
   auto fill_p_sums = [&](const char* rt, float kk, float cbv) {
-    const uint4* vt = reinterpret_cast<const uint4*>(rt);
-    int u = u0 + ctid;
-    for (; u + 7 * kCT < u1; u += 8 * kCT) {
+    const uint4* vt = reinterpret_cast<const uint4*>(rt) + u0;
+    int base = 0;
+    for (; base + 8 * kCT <= cu; base += 8 * kCT) {
       uint4 t[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) t[j] = ld_stream_v4(vt + u + j * kCT);
+      for (int j = 0; j < 8; ++j) t[j] = ld_stream_v4(vt + base + ctid + j * kCT);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) usum[u + j * kCT - u0] = p_vec_sum<BF16>(t[j], kk, cbv);
+      for (int j = 0; j < 8; ++j) {
+        const float g = group_sum(p_vec_sum<BF16>(t[j], kk, cbv));
+        if ((ctid & (kGrp - 1)) == 0) usum[(base + ctid + j * kCT) / kGrp] = g;
+      }
     }
-    for (; u < u1; u += kCT) usum[u - u0] = p_vec_sum<BF16>(ld_stream_v4(vt + u), kk, cbv);
+    for (; base < cu; base += kCT) {             // uniform trip count: every lane shuffles
+      const int uu = base + ctid;
+      const float g = group_sum(uu < cu ? p_vec_sum<BF16>(ld_stream_v4(vt + uu), kk, cbv) : 0.0f);
+      if ((ctid & (kGrp - 1)) == 0 && uu < cu) usum[uu / kGrp] = g;
+    }
   };
 
   // One cluster exchange (consumer warp 0 pushes and combines; every consumer thread calls it).
@@ -556,21 +537,25 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     if (cw == 0) {
       // The pending position's CTA residual total (its warp partials are ordered by the barrier
       // every consumer passed before this exchange).
-      const float pw = pv ? warp_sum_lane0(lane < kCW ? sm.wsum2[lane] : 0.0f) : 0.0f;
+      // Reductions over the kCW warp partials (lanes below kCW), then broadcast from lane 0 to the
+      // lanes that push.
+      const float pw = pv ? __shfl_sync(kFull, lanes_sum(lane < kCW ? sm.wsum2[lane] : 0.0f, kCW), 0) : 0.0f;
       float4 rec = make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
       int rbad = 0;
       if (has_cur) {
         if (kind == kArgmax) {
           float v = lane < kCW ? sm.wpart[lane].x : -INFINITY;
           int ii = lane < kCW ? sm.widx[lane] : INT_MAX;
-          warp_argmax(v, ii);
-          rec = make_float4(v, __int_as_float(ii), 0.0f, 0.0f);
+          lanes_argmax(v, ii, kCW);
+          rec = make_float4(__shfl_sync(kFull, v, 0), __int_as_float(__shfl_sync(kFull, ii, 0)), 0.0f, 0.0f);
         } else {
           const float4 w = lane < kCW ? sm.wpart[lane] : make_float4(-INFINITY, 0.0f, -INFINITY, 0.0f);
-          const float Mct = warp_max(w.x), Mcd = warp_max(w.z);
+          const float Mct = lanes_max(w.x, kCW), Mcd = lanes_max(w.z, kCW);
           const float a = (w.y > 0.0f) ? w.y * ex2((w.x - Mct) * k) : 0.0f;
           const float c = (w.w > 0.0f) ? w.w * ex2((w.z - Mcd) * k) : 0.0f;
-          rec = make_float4(Mct, warp_sum_lane0(a), Mcd, warp_sum_lane0(c));
+          const float sa = lanes_sum(a, kCW), sc = lanes_sum(c, kCW);
+          rec = make_float4(__shfl_sync(kFull, Mct, 0), __shfl_sync(kFull, sa, 0),
+                            __shfl_sync(kFull, Mcd, 0), __shfl_sync(kFull, sc, 0));
         }
         rbad = __any_sync(kFull, lane < kCW && sm.wbad[lane]);
       }
@@ -590,7 +575,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       if (has_cur && kind == kArgmax) {
         float v = lane < C ? r.x : -INFINITY;
         int ii = lane < C ? __float_as_int(r.y) : INT_MAX;
-        warp_argmax(v, ii);
+        lanes_argmax(v, ii, C);
         if (lane == 0) {
           sm.bad = gbad || !(v > -INFINITY);
           sm.cand = ii;
@@ -598,17 +583,17 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
         }
       } else if (has_cur) {
         // Global max and normaliser of p (and q); the chunk-level CDF of p by an inclusive scan.
-        const float Mt = warp_max(r.x), Md = warp_max(r.z);
+        const float Mt = lanes_max(r.x, C), Md = lanes_max(r.z, C);
         const float term_t = (lane < C && r.y > 0.0f) ? r.y * ex2((r.x - Mt) * k) : 0.0f;
-        const float incl_t = warp_incl_scan(term_t, lane);
-        const float St = __shfl_sync(kFull, incl_t, 31);
+        const float incl_t = lanes_incl_scan(term_t, lane, C);
+        const float St = __shfl_sync(kFull, incl_t, C - 1);
         float excl_t = __shfl_up_sync(kFull, incl_t, 1);
         if (lane == 0) excl_t = 0.0f;
         bool b2 = gbad || !(Mt > -INFINITY && Mt < INFINITY);
         float Sd = 1.0f;
         if (kind == kVerify) {
           const float term_d = (lane < C && r.w > 0.0f) ? r.w * ex2((r.z - Md) * k) : 0.0f;
-          Sd = __shfl_sync(kFull, warp_incl_scan(term_d, lane), 31);
+          Sd = __shfl_sync(kFull, lanes_incl_scan(term_d, lane, C), C - 1);
           b2 = b2 || !(Md > -INFINITY && Md < INFINITY);
         }
         // Chunk of a draw from p with threshold t (the bonus draw, or the residual fallback).
@@ -652,8 +637,8 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
         // inclusive prefix first exceeds u * W ([R] One round, step 4), else (rounding) the last
         // positive chunk; with no residual mass at all, the draw from p picked at its exchange.
         const float w_r = lane < C ? __uint_as_float(au.y) : 0.0f;
-        const float incl_w = warp_incl_scan(w_r, lane);
-        const float Wt = __shfl_sync(kFull, incl_w, 31);
+        const float incl_w = lanes_incl_scan(w_r, lane, C);
+        const float Wt = __shfl_sync(kFull, incl_w, C - 1);
         float excl_w = __shfl_up_sync(kFull, incl_w, 1);
         if (lane == 0) excl_w = 0.0f;
         const float t = sm.pend.u_res * Wt;
@@ -745,7 +730,6 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     }
 
     // ---- pass 1 out of the ring ----
-    const bool kept = kind == kBonus && !pv;   // pass 1 keeps the bonus draw's vector sums
     const float k = p.greedy ? 0.0f : kLog2e / p.T;
     float mt = -INFINITY, md = -INFINITY, mxt = -INFINITY, mxd = -INFINITY;
     f32x2 st = pk(0.0f, 0.0f), sd = pk(0.0f, 0.0f);
@@ -761,23 +745,20 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
           constexpr int N = kSlotUnits / kCT;
           const uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
           uint4 v[N];
+          if (nu == kSlotUnits) {      // a full slot: no tail to mask
 #pragma unroll
-          for (int j = 0; j < N; ++j) {
-            const int uu = ctid + j * kCT;
-            v[j] = uu < nu ? src[uu] : make_uint4(ninf, ninf, ninf, ninf);
+            for (int j = 0; j < N; ++j) v[j] = src[ctid + j * kCT];
+          } else {
+#pragma unroll
+            for (int j = 0; j < N; ++j) {
+              const int uu = ctid + j * kCT;
+              v[j] = uu < nu ? src[uu] : make_uint4(ninf, ninf, ninf, ninf);
+            }
           }
           if (kind == kArgmax) {
 #pragma unroll
             for (int j = 0; j < N; ++j)
               argmax_update<BF16>(v[j], (u0 + ks * kSlotUnits + ctid + j * kCT) * E, mt, idx, mxt);
-          } else if (row == 0 && kind == kBonus && !pv) {
-            // Keep each vector's p sum and the batch's reference max for the bonus draw.
-            float vs[N];
-            online_update_batch_keep<BF16, N>(v, k, mt, st, mxt, vs);
-#pragma unroll
-            for (int j = 0; j < N; ++j)
-              if (ctid + j * kCT < nu) usum[ks * kSlotUnits + ctid + j * kCT] = vs[j];
-            bref[ks * kCT + ctid] = mt;
           } else if (row == 0) {
             online_update_batch<BF16, N>(v, k, mt, st, mxt);
           } else {
@@ -868,17 +849,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
           if (cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagAccept, 0.0f, 0.0f, 0.0f, lane);
           continue;
         }
-        if (kept) {
-          // Rescale this thread's vector sums from pass 1 (kept against the batch's running max)
-          // to the global max: weight exp2(z k + cb), cb = -M k.
-          for (int ks = 0; ks < nsl; ++ks) {
-            const float f = ex2(fmaf(bref[ks * kCT + ctid], kk, cb));
-            const int nu = min(kSlotUnits, cu - ks * kSlotUnits);
-            for (int uu = ctid; uu < nu; uu += kCT) usum[ks * kSlotUnits + uu] *= f;
-          }
-        } else {
-          fill_p_sums(rowt, kk, cb);
-        }
+        fill_p_sums(rowt, kk, cb);
         named_bar_sync(kConsumerBar, kCT);
         int finisher = 0;
         const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm, ctid,
@@ -897,15 +868,21 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       bool tmo = false;
       for (int ks = 0; ks < nsl2; ++ks, ++tc) {
         const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
-        if (!mbar_wait(smem_addr(&sm.full[slot]), par)) tmo = true;
+        // Warp-uniform, so that a wait given up by one lane cannot split a group's shuffle.
+        if (!__all_sync(kFull, mbar_wait(smem_addr(&sm.full[slot]), par))) tmo = true;
         const int nu = min(kHalfUnits, cu - ks * kHalfUnits);
         const uint4* st4 = ringv + slot * kSlotUnits;
         const uint4* sd4 = st4 + kHalfUnits;
         if (!cbad && !tmo) {
-          for (int uu = ctid; uu < nu; uu += kCT) {
-            const float sv = resid_vec_sum<BF16>(st4[uu], sd4[uu], k2, c2);
-            usum[ks * kHalfUnits + uu] = sv;
+          // Uniform trip count over the slot (kHalfUnits is a multiple of kCT): every lane of a
+          // group takes part in the shuffle; lanes past the chunk's end add zero.
+#pragma unroll
+          for (int j = 0; j < kHalfUnits / kCT; ++j) {
+            const int uu = ctid + j * kCT;
+            const float sv = uu < nu ? resid_vec_sum<BF16>(st4[uu], sd4[uu], k2, c2) : 0.0f;
             W += sv;
+            const float g = group_sum(sv);
+            if ((ctid & (kGrp - 1)) == 0 && uu < nu) usum[(ks * kHalfUnits + uu) / kGrp] = g;
           }
         }
         __syncwarp();
