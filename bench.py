@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--onehot", action="store_true",
+                    help="one-hot drafts (greedy drafter): time spec_verify_onehot, no draft logits")
     return ap.parse_args()
 
 
@@ -142,39 +144,44 @@ def workload_for(args, rank):
 # CPU baseline: the fp64 oracle, as it stands, on a bounded sample of the same workload
 # ------------------------------------------------------------------------------------------------
 
-def oracle_pool(cfg_key, seconds, seed=12345):
+def _oracle(w, onehot):
+    from oracle.spec_verify_oracle import oracle_verify, oracle_verify_onehot
+    if onehot:
+        return oracle_verify_onehot(w.target_logits, w.draft_tokens, w.draft_len, w.temperature,
+                                    w.uniforms)
+    return oracle_verify(w.target_logits, w.draft_logits, w.draft_tokens, w.draft_len,
+                         w.temperature, w.uniforms)
+
+
+def oracle_pool(cfg_key, seconds, seed=12345, onehot=False):
     """Rows of the workload drawn on the host (numpy backend), as many as the oracle verifies in
     about `seconds` of single-thread CPU time (calibrated on 8 rows). Input generation is untimed."""
     import dataclasses
 
     import numpy as np
 
-    from oracle.spec_verify_oracle import oracle_verify
     from workloads import get_config, make_workload
     cfg = get_config(cfg_key)
     probe = make_workload(dataclasses.replace(cfg, B=8), seed=seed, backend="numpy")
     t0 = time.perf_counter()
-    oracle_verify(probe.target_logits, probe.draft_logits, probe.draft_tokens, probe.draft_len,
-                  probe.temperature, probe.uniforms)
+    _oracle(probe, onehot)
     t8 = time.perf_counter() - t0
     rows = int(max(8, min(cfg.B, round(seconds / max(t8, 1e-6) * 8 / 8) * 8)))
     w = make_workload(dataclasses.replace(cfg, B=rows), seed=seed + 1, backend="numpy")
     return w, int(np.sum(w.draft_len.astype(np.int64) + 1))
 
 
-def oracle_run(w):
+def oracle_run(w, onehot=False):
     """Wall seconds of one oracle pass over the pool's rows."""
-    from oracle.spec_verify_oracle import oracle_verify
     t0 = time.perf_counter()
-    oracle_verify(w.target_logits, w.draft_logits, w.draft_tokens, w.draft_len, w.temperature,
-                  w.uniforms)
+    _oracle(w, onehot)
     return time.perf_counter() - t0
 
 
-def oracle_sample_rate(cfg_key, seconds):
+def oracle_sample_rate(cfg_key, seconds, onehot=False):
     """Oracle throughput (positions/s) on a bounded host-drawn sample of the workload."""
-    w, pos = oracle_pool(cfg_key, seconds)
-    secs = oracle_run(w)
+    w, pos = oracle_pool(cfg_key, seconds, onehot=onehot)
+    secs = oracle_run(w, onehot)
     return pos / secs, w.B, pos, secs
 
 
@@ -187,19 +194,20 @@ def run_reference(args):
     from workloads import get_config
     cfg = get_config(args.workload)
     per_step = 1.5      # seconds of single-thread oracle work per step
-    w, pos = oracle_pool(args.workload, per_step)
+    w, pos = oracle_pool(args.workload, per_step, onehot=args.onehot)
     for _ in range(args.warmup):
-        oracle_run(w)
+        oracle_run(w, args.onehot)
     total = 0.0
     for _ in range(args.steps):
-        total += oracle_run(w)
+        total += oracle_run(w, args.onehot)
     value = pos * args.steps / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": cfg.name, "B": cfg.B, "gamma_max": cfg.gamma_max, "V": cfg.V,
+        "config": {"workload": cfg.name + ("_onehot_drafts" if args.onehot else ""), "B": cfg.B,
+                   "gamma_max": cfg.gamma_max, "V": cfg.V,
                    "logits": cfg.dtype, "sample_rows_per_step": w.B,
                    "sample_positions_per_step": pos},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
@@ -236,9 +244,21 @@ def run_gpu(args):
     out_num = torch.empty((B,), dtype=torch.int32, device=dev)
     out_alpha = torch.empty((B, G), dtype=torch.float32, device=dev)
 
+    if args.onehot:                  # one-hot drafts: no draft logits exist
+        del t["draft_logits"]
+
+    def call(inp):
+        if args.onehot:
+            sv.spec_verify_onehot(inp["target_logits"], inp["draft_tokens"], inp["draft_len"],
+                                  inp["temperature"], inp["uniforms"], out_tokens, out_num,
+                                  out_alpha, None, None, ws, stream)
+        else:
+            sv.spec_verify(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
+                           inp["draft_len"], inp["temperature"], inp["uniforms"], out_tokens,
+                           out_num, out_alpha, ws, stream)
+
     def step():
-        sv.spec_verify(t["target_logits"], t["draft_logits"], t["draft_tokens"], t["draft_len"],
-                       t["temperature"], t["uniforms"], out_tokens, out_num, out_alpha, ws, stream)
+        call(t)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -269,14 +289,15 @@ def run_gpu(args):
         ms_step = float(mt.item())
     positions = w.positions()
     value = positions * world / (ms_step * 1e-3)
-    algo_bytes = w.algorithmic_bytes()
+    algo_bytes = w.algorithmic_bytes(onehot=args.onehot)
     achieved_gbs = algo_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
 
     traffic = None
     if TRAFFIC_FILE.exists():
         tr = json.loads(TRAFFIC_FILE.read_text())
-        if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == cfg.name:
+        if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == cfg.name \
+                and not args.onehot:
             traffic = tr["bytes_per_full_launch"]
 
     # ---- end to end: pinned host inputs -> device, the call, outputs -> pinned host ----
@@ -293,9 +314,7 @@ def run_gpu(args):
         def e2e_step():
             for k in host:
                 dev_in[k].copy_(host[k], non_blocking=True)
-            sv.spec_verify(dev_in["target_logits"], dev_in["draft_logits"], dev_in["draft_tokens"],
-                           dev_in["draft_len"], dev_in["temperature"], dev_in["uniforms"],
-                           out_tokens, out_num, out_alpha, ws, stream)
+            call(dev_in)
             h_tok.copy_(out_tokens, non_blocking=True)
             h_num.copy_(out_num, non_blocking=True)
             h_alpha.copy_(out_alpha, non_blocking=True)
@@ -323,7 +342,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        rate, rows, pos, secs = oracle_sample_rate(args.workload, args.cpu_seconds)
+        rate, rows, pos, secs = oracle_sample_rate(args.workload, args.cpu_seconds, args.onehot)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{rows} rows ({pos} positions) of the workload drawn on the host, "
                          f"{secs:.1f} s of single-thread fp64 oracle work"}
@@ -333,7 +352,8 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-            "config": {"workload": cfg.name, "B": B, "gamma_max": G, "V": V, "logits": cfg.dtype,
+            "config": {"workload": cfg.name + ("_onehot_drafts" if args.onehot else ""), "B": B,
+                       "gamma_max": G, "V": V, "logits": cfg.dtype,
                        "greedy_rows": int((w.temperature == 0).sum()),
                        "positions_per_gpu": positions, "padded_positions_per_gpu": B * (G + 1),
                        "algorithmic_bytes_per_step": algo_bytes,

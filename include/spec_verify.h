@@ -122,6 +122,26 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
                    int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                    void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* Verification of one-hot drafts: the drafter decoded greedily, so its distribution at position i is
+ * q_i = [v == x_i] and no draft logits exist. [B] "Inference: distillation and speculative decoding",
+ * brunomaga.github.io -- Draft-model speculative decoding (a greedy draft is the one-hot case: the
+ * target keeps it with probability p(x) and on a rejection draws from p without x); [R] One round,
+ * steps 3-5 with that q. Per sampled position i < gamma_b:
+ *   keep x_i while u[b,i] < p_i(x_i); alpha_i = sum_v min(p_i(v), q_i(v)) = p_i(x_i);
+ *   at the first rejection the replacement is drawn with u[b,G] from max(0, p - q), i.e. p with x
+ *   left out (inverse CDF in index order, strict '>' against u times its mass); a bonus token as in
+ *   spec_verify. Greedy rows (temperature 0) are verified exactly as in spec_verify.
+ * Arguments, layout, ownership, workspace and errors as in spec_verify_ex without draft_logits;
+ * out_q_draft receives 1 for every verified position. Only rows of 16-byte multiples with a 16-byte
+ * aligned target_logits are supported: other V return SV_ERR_BAD_SHAPE, a misaligned pointer
+ * SV_ERR_MISALIGNED. Only the target rows 0..gamma_b of each row are read. */
+int spec_verify_onehot(const void* target_logits, const int32_t* draft_tokens,
+                       const int32_t* draft_len, const float* temperature, const float* uniforms,
+                       int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                       float* out_p_draft, float* out_q_draft,
+                       int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                       void* workspace, size_t workspace_bytes, void* cuda_stream);
+
 /* spec_verify_ex for callers that cannot allocate device memory. The pages have no counterpart:
  * this is a deployment convenience, not part of the method.
  *

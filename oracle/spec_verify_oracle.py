@@ -20,6 +20,8 @@ What it computes, and where the pages define it (page title, then section):
   - Knowledge distillation: the temperature softmax.
 * [C] "Speculative decoding", cgnarendiran.github.io blog, The correction that makes it exact:
   the accept probability and the normalised residual.
+* One-hot drafts ([B] Draft-model speculative decoding, the greedy-drafter special case):
+  ``oracle_verify_onehot`` is the same verification with q_i = [v == x_i].
 
 Parity status: every function below is pinned by the tests in ``tests/test_oracle.py`` and
 ``tests/test_montecarlo.py`` (page-printed worked examples, closed forms, identities, an exact
@@ -293,6 +295,54 @@ def oracle_verify(target_logits, draft_logits, draft_tokens, draft_len, temperat
     results = [None] * B
     for b in (range(B) if rows is None else rows):
         zd = draft_logits[b] if draft_logits is not None else np.zeros((G, V))
+        r = verify_row(target_logits[b], zd, draft_tokens[b], int(draft_len[b]),
+                       np.float32(temperature[b]), uniforms[b], G, diagnostics=diagnostics, eps=eps)
+        results[b] = r
+        if r.valid:
+            out_tokens[b, :len(r.tokens)] = r.tokens
+            out_num[b] = len(r.tokens)
+            out_alpha[b] = r.alpha
+            out_p[b] = r.p_draft
+            out_q[b] = r.q_draft
+    return BatchResult(out_tokens, out_num, out_alpha, out_p, out_q, results)
+
+
+# ----------------------------------------------------------------------------------------------
+# One-hot drafts (a greedy drafter): q_i = [v == x_i]
+# ----------------------------------------------------------------------------------------------
+
+def onehot_draft_logits(x, G, V):
+    """Draft logits whose temperature softmax is one-hot at the drafted token: -inf everywhere and 0
+    at x_i ([B] Draft-model speculative decoding: greedy drafts are the special case of a one-hot
+    draft distribution). A drafted token outside [0, V) leaves its row all -inf (the row check
+    reports the token first)."""
+    zd = np.full((G, V), -np.inf)
+    for i in range(G):
+        xi = int(x[i])
+        if 0 <= xi < V:
+            zd[i, xi] = 0.0
+    return zd
+
+
+def oracle_verify_onehot(target_logits, draft_tokens, draft_len, temperature, uniforms,
+                         rows=None, diagnostics=False, eps=MARGIN):
+    """Verification of one-hot drafts: oracle_verify with q_i = [v == x_i] at every drafted position
+    (built row by row). With that q the rule keeps x with probability min(1, p(x)/1) = p(x), gives
+    alpha = sum min(p, q) = p(x), and draws a replacement from max(0, p - q), which is p without x
+    ([B] Draft-model speculative decoding)."""
+    target_logits = np.asarray(target_logits)
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    if draft_len is None:
+        draft_len = np.full(B, G, dtype=np.int64)
+    out_tokens = np.full((B, G + 1), -1, dtype=np.int32)
+    out_num = np.full(B, -1, dtype=np.int32)
+    out_alpha = np.zeros((B, G))
+    out_p = np.zeros((B, G))
+    out_q = np.zeros((B, G))
+    results = [None] * B
+    for b in (range(B) if rows is None else rows):
+        zd = onehot_draft_logits(draft_tokens[b], G, V)
         r = verify_row(target_logits[b], zd, draft_tokens[b], int(draft_len[b]),
                        np.float32(temperature[b]), uniforms[b], G, diagnostics=diagnostics, eps=eps)
         results[b] = r

@@ -24,8 +24,9 @@ STATUS_NAMES = {
 SV_ERR_SCRATCH_TOO_SMALL = 8
 SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
-EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_workspace_size",
-            "spec_verify_workspace_status", "spec_verify_status_string", "spec_verify_version")
+EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_onehot",
+            "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
+            "spec_verify_version")
 
 _lib = None
 _lock = threading.Lock()
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_ex.restype = ctypes.c_int
             L.spec_verify_noalloc.argtypes = common + [f32p, f32p, i32, i32, i32, i32, vp]
             L.spec_verify_noalloc.restype = ctypes.c_int
+            L.spec_verify_onehot.argtypes = [vp, i32p, i32p, f32p, f32p, i32p, i32p, f32p, f32p, f32p] + tail
+            L.spec_verify_onehot.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
             L.spec_verify_workspace_size.restype = ctypes.c_size_t
             L.spec_verify_workspace_status.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int32), vp]
@@ -190,6 +193,36 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, draft_len, te
         raise SpecVerifyError(st, "spec_verify_noalloc")
 
 
+def spec_verify_onehot(target_logits, draft_tokens, draft_len, temperature, uniforms, out_tokens,
+                       out_num_emitted, out_alpha, out_p_draft, out_q_draft, workspace,
+                       stream=None) -> None:
+    """Calls the C ABI spec_verify_onehot (one-hot drafts, no draft logits) on torch tensors.
+    Raises SpecVerifyError on a nonzero status."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    _check(target_logits, "target_logits", device=dev)
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, G), dev)
+    _check(draft_len, "draft_len", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, G + 2), dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B, G + 1), dev)
+    _check(out_num_emitted, "out_num_emitted", torch.int32, (B,), dev)
+    for name, t in (("out_alpha", out_alpha), ("out_p_draft", out_p_draft),
+                    ("out_q_draft", out_q_draft)):
+        _check(t, name, torch.float32, (B, G), dev)
+    _check(workspace, "workspace", device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().spec_verify_onehot(
+        _ptr(target_logits), _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature),
+        _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted), _ptr(out_alpha),
+        _ptr(out_p_draft), _ptr(out_q_draft), B, G, V, _dtype_code(target_logits),
+        _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_onehot")
+
+
 def spec_verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
                 out_tokens, out_num_emitted, out_alpha, workspace, stream=None) -> None:
     """Calls the C ABI spec_verify on torch tensors (see spec_verify_ex)."""
@@ -214,8 +247,9 @@ def workspace_for(B, G, V, dtype_code, device, stream=None):
 
 
 def verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
-           with_probs=False, stream=None):
-    """Allocates the outputs, runs spec_verify(_ex) and returns
+           with_probs=False, stream=None, onehot=False):
+    """Allocates the outputs, runs spec_verify(_ex) (or spec_verify_onehot when ``onehot``: the
+    drafts are one-hot and draft_logits is ignored) and returns
     (out_tokens [B, G+1], out_num_emitted [B], out_alpha [B, G][, out_p, out_q])."""
     import torch
     B, G1, V = target_logits.shape
@@ -227,8 +261,12 @@ def verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, un
     out_p = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
     out_q = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
     ws = workspace_for(B, G, V, _dtype_code(target_logits), dev, stream)
-    spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
-                   out_tokens, out_num, out_alpha, out_p, out_q, ws, stream)
+    if onehot:
+        spec_verify_onehot(target_logits, draft_tokens, draft_len, temperature, uniforms,
+                           out_tokens, out_num, out_alpha, out_p, out_q, ws, stream)
+    else:
+        spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                       out_tokens, out_num, out_alpha, out_p, out_q, ws, stream)
     if with_probs:
         return out_tokens, out_num, out_alpha, out_p, out_q
     return out_tokens, out_num, out_alpha

@@ -140,18 +140,24 @@ int spec_verify_workspace_status(const void* workspace, int32_t B, int32_t gamma
   return SV_OK;
 }
 
-int spec_verify_ex(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
-                   const int32_t* draft_len, const float* temperature, const float* uniforms,
-                   int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
-                   float* out_p_draft, float* out_q_draft,
-                   int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
-                   void* workspace, size_t workspace_bytes, void* cuda_stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation, planning and launch shared by spec_verify_ex (draft logits) and spec_verify_onehot
+// (one-hot drafts: no draft logits, 16-byte rows only).
+int verify_impl(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                const int32_t* draft_len, const float* temperature, const float* uniforms,
+                int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                float* out_p_draft, float* out_q_draft,
+                int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                void* workspace, size_t workspace_bytes, void* cuda_stream, bool onehot) {
   if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
   if (!sizes_ok(B, gamma_max, V, dtype)) return SV_ERR_BAD_SHAPE;
   const int G = gamma_max;
   if (!target_logits || !temperature || !uniforms || !out_tokens || !out_num_emitted)
     return SV_ERR_NULL_POINTER;
-  if (G > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_NULL_POINTER;
+  if (G > 0 && ((!onehot && !draft_logits) || !draft_tokens)) return SV_ERR_NULL_POINTER;
   const bool bf16 = dtype == SV_DTYPE_BF16;
   const uintptr_t es = bf16 ? 2 : 4;
   auto mis = [](const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; };
@@ -166,6 +172,8 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   const bool vec = (static_cast<size_t>(V) * es) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
                    (!draft_logits || reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0);
+  if (onehot && !vec)   // one-hot drafts run on the streaming kernel only
+    return (static_cast<size_t>(V) * es) % 16 != 0 ? SV_ERR_BAD_SHAPE : SV_ERR_MISALIGNED;
   int vpt_index = 0, eC = 1, eper = 1;
   if (!vec && !element_plan(V, &vpt_index, &eC, &eper)) return SV_ERR_BAD_SHAPE;
   const int sC = vec ? stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es)) : 0;
@@ -175,9 +183,10 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   const int dev_status = check_device(&dev);
   if (dev_status != SV_OK) return dev_status;
 
-  sv::Params P;
+  sv::Params P{};
+  P.onehot = onehot ? 1 : 0;
   P.zt = target_logits;
-  P.zd = draft_logits;
+  P.zd = onehot ? nullptr : draft_logits;
   P.tokens = draft_tokens;
   P.draft_len = draft_len;
   P.temperature = temperature;
@@ -214,6 +223,32 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
   P.nclusters = B * (G + 1);
   if (sv::launch_element(P, bf16, vpt_index, stream) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_ex(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                   const int32_t* draft_len, const float* temperature, const float* uniforms,
+                   int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                   float* out_p_draft, float* out_q_draft,
+                   int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                   void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return verify_impl(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                     out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft, B, gamma_max,
+                     V, dtype, workspace, workspace_bytes, cuda_stream, false);
+}
+
+int spec_verify_onehot(const void* target_logits, const int32_t* draft_tokens,
+                       const int32_t* draft_len, const float* temperature, const float* uniforms,
+                       int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
+                       float* out_p_draft, float* out_q_draft,
+                       int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                       void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  return verify_impl(target_logits, nullptr, draft_tokens, draft_len, temperature, uniforms,
+                     out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft, B, gamma_max,
+                     V, dtype, workspace, workspace_bytes, cuda_stream, true);
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,

@@ -26,7 +26,7 @@ constexpr int kMaxCluster = 16;
 // residual sums must fit in shared memory beside the copy ring.
 constexpr int kStreamMaxUnits = 4864;
 
-enum : int { kVerify = 0, kBonus = 1, kArgmax = 2 };
+enum : int { kVerify = 0, kBonus = 1, kArgmax = 2, kOneHot = 3 };
 enum : int { kFlagAccept = 1, kFlagBad = 2, kFlagDone = 4 };
 
 struct Params {
@@ -49,6 +49,7 @@ struct Params {
   int units;                 // load units per row (16-byte vectors, or logits on the element path)
   int per;                   // units per CTA chunk
   int nclusters;             // clusters in the grid (persistent kernel)
+  int onehot;                // drafted positions have one-hot drafts q = [v == x] (no draft logits)
 };
 
 // ------------------------------------------------------------------------------------------------

@@ -106,6 +106,7 @@ struct Shared {
   float k, ct, cd, cb;               // log2(e)/T; exponent offsets of p, q and of unnormalised p
   float px, qx, t_local, p_tlocal;
   int acc, bad, cand, draw_chunk, p_chunk;
+  int resid_mass;                    // one-hot drafts: p without x has positive mass
   // ... and the pending drafted position whose residual totals this exchange carried
   float pend_alpha, pend_tlocal;
   int pend_chunk, pend_resid;
@@ -125,7 +126,7 @@ struct Shared {
 struct Pos {
   int b, i, gb;
   float T;
-  bool len_ok, t_ok, greedy, load, two;
+  bool len_ok, t_ok, greedy, load, two, oh;   // two: a draft row is read; oh: one-hot draft
 };
 
 // Slot s in position-major order (s = i * B + b): the slots a cluster strides over mix every
@@ -141,7 +142,8 @@ __device__ __forceinline__ Pos classify(const Params& P, int s) {
   p.greedy = (p.T == 0.0f);
   p.t_ok = p.greedy || (p.T >= FLT_MIN && p.T <= FLT_MAX);   // NaN fails both
   p.load = p.len_ok && p.t_ok && p.i <= p.gb;
-  p.two = p.load && !p.greedy && p.i < p.gb;
+  p.two = p.load && !p.greedy && p.i < p.gb && !P.onehot;
+  p.oh = p.load && !p.greedy && p.i < p.gb && P.onehot;
   return p;
 }
 
@@ -278,6 +280,22 @@ __device__ __forceinline__ float p_vec_sum(const uint4& t, float k, float cb) {
   return s;
 }
 
+// The vector with element e set to -inf (a one-hot draft's token, left out of a sum).
+template <bool BF16>
+__device__ __forceinline__ uint4 mask_elem(uint4 v, int e) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (BF16) {
+      if (e == 2 * q) w[q] = (w[q] & 0xffff0000u) | 0xff80u;
+      if (e == 2 * q + 1) w[q] = (w[q] & 0x0000ffffu) | 0xff800000u;
+    } else if (e == q) {
+      w[q] = 0xff800000u;
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // Sum over the kGrp consecutive lanes of a group (vectors u, u+1, ... of a chunk sit in
 // consecutive lanes); every lane of the group gets the total.
 __device__ __forceinline__ float group_sum(float v) {
@@ -290,11 +308,12 @@ __device__ __forceinline__ float group_sum(float v) {
 // (residual or p weights, per `resid`); the token is the first logit whose running weight exceeds
 // t_local, else (rounding) the last logit with positive weight. Block-wide prefix sum over the
 // group sums, then one reload of the crossing group. Returns the token in warp `finisher` (all its
-// lanes); other warps return -1. All consumer threads call it.
+// lanes); other warps return -1. All consumer threads call it. Token `skip_tok` (if >= 0) has weight 0
+// (the usum entries already leave it out).
 template <bool BF16>
 __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, const char* rowt,
                           const char* rowd, bool resid, float k, float ct, float cd, float cb,
-                          Shared& sm, int ctid, int& finisher) {
+                          Shared& sm, int ctid, int& finisher, int skip_tok = -1) {
   constexpr int E = BF16 ? 8 : 4;
   const int lane = ctid & 31, cw = ctid >> 5;
   const int cg = (cu + kGrp - 1) / kGrp;
@@ -372,7 +391,8 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
     float c = before;
     int pick = -1, lastp = -1;
     for (int u = ga; u < gz && (pick < 0 || overrun); ++u) {
-      const uint4 t = ld_stream_v4(reinterpret_cast<const uint4*>(rowt) + u);
+      uint4 t = ld_stream_v4(reinterpret_cast<const uint4*>(rowt) + u);
+      if (skip_tok >= 0 && u == skip_tok / E) t = mask_elem<BF16>(t, skip_tok - u * E);   // weight 0
       const uint4 d = resid ? ld_stream_v4(reinterpret_cast<const uint4*>(rowd) + u) : t;
 #pragma unroll
       for (int e = 0; e < E; e += 2) {
@@ -506,14 +526,19 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
   // after which its draw (if rejected) and finish happen. Uniform across the cluster.
   bool pv = false;                 // a pending position exists (its fields are in sm.pend)
 
-  // Group sums of p's unnormalised weights exp2(z k + cb) over this CTA's chunk, from L2.
-  auto fill_p_sums = [&](const char* rt, float kk, float cbv) {
+  // Group sums of p's unnormalised weights exp2(z k + cb) over this CTA's chunk, from L2; token
+  // `excl` (if >= 0) left out.
+  auto fill_p_sums = [&](const char* rt, float kk, float cbv, int excl) {
     const uint4* vt = reinterpret_cast<const uint4*>(rt) + u0;
+    const int xu = excl >= 0 ? excl / E - u0 : -1;     // the chunk-local vector holding excl
     int base = 0;
     for (; base + 8 * kCT <= cu; base += 8 * kCT) {
       uint4 t[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) t[j] = ld_stream_v4(vt + base + ctid + j * kCT);
+      for (int j = 0; j < 8; ++j) {
+        t[j] = ld_stream_v4(vt + base + ctid + j * kCT);
+        if (base + ctid + j * kCT == xu) t[j] = mask_elem<BF16>(t[j], excl - (u0 + xu) * E);
+      }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float g = group_sum(p_vec_sum<BF16>(t[j], kk, cbv));
@@ -522,7 +547,13 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     }
     for (; base < cu; base += kCT) {             // uniform trip count: every lane shuffles
       const int uu = base + ctid;
-      const float g = group_sum(uu < cu ? p_vec_sum<BF16>(ld_stream_v4(vt + uu), kk, cbv) : 0.0f);
+      float sv = 0.0f;
+      if (uu < cu) {
+        uint4 t = ld_stream_v4(vt + uu);
+        if (uu == xu) t = mask_elem<BF16>(t, excl - (u0 + xu) * E);
+        sv = p_vec_sum<BF16>(t, kk, cbv);
+      }
+      const float g = group_sum(sv);
       if ((ctid & (kGrp - 1)) == 0 && uu < cu) usum[uu / kGrp] = g;
     }
   };
@@ -583,13 +614,20 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
         }
       } else if (has_cur) {
         // Global max and normaliser of p (and q); the chunk-level CDF of p by an inclusive scan.
-        const float Mt = lanes_max(r.x, C), Md = lanes_max(r.z, C);
+        // One-hot drafts: the chunks' sums leave x out (the residual p without x, chunk by chunk);
+        // x's own term joins the normaliser, against a reference no lower than z(x).
+        float Mt = lanes_max(r.x, C);
+        const float Md = lanes_max(r.z, C);
+        const bool oh = kind == kOneHot;
+        if (oh && zx_t > Mt && zx_t < INFINITY) Mt = zx_t;
         const float term_t = (lane < C && r.y > 0.0f) ? r.y * ex2((r.x - Mt) * k) : 0.0f;
         const float incl_t = lanes_incl_scan(term_t, lane, C);
-        const float St = __shfl_sync(kFull, incl_t, C - 1);
+        const float ex_x = oh ? ex2((zx_t - Mt) * k) : 0.0f;   // x's unnormalised weight
+        const float St = __shfl_sync(kFull, incl_t, C - 1) + ex_x;
         float excl_t = __shfl_up_sync(kFull, incl_t, 1);
         if (lane == 0) excl_t = 0.0f;
         bool b2 = gbad || !(Mt > -INFINITY && Mt < INFINITY);
+        if (oh) b2 = b2 || (zx_t != zx_t) || zx_t == INFINITY;   // x's logit was left out of the scan
         float Sd = 1.0f;
         if (kind == kVerify) {
           const float term_d = (lane < C && r.w > 0.0f) ? r.w * ex2((r.z - Md) * k) : 0.0f;
@@ -605,8 +643,13 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
           return c;
         };
         float tl_b = 0.0f, tl_p = 0.0f;
-        const int cb_chunk = chunk_of(u_bon * St, tl_b);   // [R] One round, step 5
-        const int cp_chunk = chunk_of(u_res * St, tl_p);   // zero-residual fallback
+        // Bonus ([R] One round, step 5); one-hot drafts: the residual p without x, whose chunk CDF
+        // is the scan itself ([R] One round, step 4 with q = [v == x]).
+        const float Wr = __shfl_sync(kFull, incl_t, C - 1);
+        const int cb_chunk = chunk_of(oh ? u_res * Wr : u_bon * St, tl_b);
+        // Zero-residual fallback: the draw from p with u[G]; for one-hot drafts p without x has no
+        // mass, so that draw is x itself.
+        const int cp_chunk = chunk_of(u_res * St, tl_p);
         if (lane == 0) {
           const float ct = -fmaf(Mt, k, log2f(St));
           const float cd = -fmaf(Md, k, log2f(Sd));
@@ -625,8 +668,15 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
             sm.px = px;
             sm.qx = qx;
             sm.acc = u_acc < ratio;
+          } else if (oh) {
+            // q(x) = 1: keep x while u < p(x); alpha = sum min(p, q) = p(x).
+            const float px = __fdividef(ex_x, St);
+            sm.px = px;
+            sm.qx = 1.0f;
+            sm.acc = u_acc < px;
+            sm.resid_mass = Wr > 0.0f;
           }
-          sm.draw_chunk = (kind == kBonus) ? cb_chunk : -1;
+          sm.draw_chunk = (kind == kBonus || oh) ? cb_chunk : -1;
           sm.t_local = tl_b;
           sm.p_chunk = cp_chunk;
           sm.p_tlocal = tl_p;
@@ -693,7 +743,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     const char* prd = sm.pend.rd;
     const float pkk = sm.pend.k, pct = sm.pend.ct, pcd = sm.pend.cd, pcb = sm.pend.cb;
     if (!resid) {
-      fill_p_sums(prt, pkk, pcb);
+      fill_p_sums(prt, pkk, pcb, -1);
       named_bar_sync(kConsumerBar, kCT);
     }
     int finisher = 0;
@@ -710,7 +760,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       continue;
     }
     const bool ok = row_scalars_ok(P, p.b, p.gb, p.greedy, lane);
-    const int kind = p.greedy ? kArgmax : (p.two ? kVerify : kBonus);
+    const int kind = p.greedy ? kArgmax : (p.two ? kVerify : (p.oh ? kOneHot : kBonus));
     const char* rowt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES;
     const char* rowd = p.two ? static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES
                              : nullptr;
@@ -722,11 +772,11 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
       const float* ur = P.uniforms + (size_t)p.b * (G + 2);
       u_res = __ldg(ur + G);
       u_bon = __ldg(ur + G + 1);
-      if (kind == kVerify) {
+      if (kind == kVerify || kind == kOneHot) {
         u_acc = __ldg(ur + p.i);
         zx_t = load_logit<BF16>(rowt, x);
-        zx_d = load_logit<BF16>(rowd, x);
       }
+      if (kind == kVerify) zx_d = load_logit<BF16>(rowd, x);
     }
 
     // ---- pass 1 out of the ring ----
@@ -754,6 +804,13 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
               const int uu = ctid + j * kCT;
               v[j] = uu < nu ? src[uu] : make_uint4(ninf, ninf, ninf, ninf);
             }
+          }
+          if (kind == kOneHot) {
+            // The drafted token's own term is added at the exchange: the chunk sums leave it out,
+            // so the residual mass of every chunk (p without x) has no cancellation.
+#pragma unroll
+            for (int j = 0; j < N; ++j)
+              if (u0 + ks * kSlotUnits + ctid + j * kCT == x / E) v[j] = mask_elem<BF16>(v[j], x % E);
           }
           if (kind == kArgmax) {
 #pragma unroll
@@ -833,6 +890,41 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     const float kk = sm.k, ct = sm.ct, cd = sm.cd, cb = sm.cb;
     const int cbad = sm.bad;
 
+    if (kind == kOneHot) {
+      // One-hot draft: finished at its exchange (alpha = p(x) needs no residual pass). On a
+      // rejection the residual p without x is drawn by the CTA holding its threshold. With no
+      // residual mass the fallback draw from p can only give x (all of p is on x).
+      const float apx = sm.px;
+      const bool rej = !(cbad || sm.acc);
+      if (!rej || !sm.resid_mass) {
+        if (rank == fin && cw == 0) {
+          if (cbad) finish_position(P, p.b, p.i, p.gb, -1, kFlagBad, 0.0f, 0.0f, 0.0f, lane);
+          else if (!rej) finish_position(P, p.b, p.i, p.gb, -1, kFlagAccept, apx, apx, 1.0f, lane);
+          else finish_position(P, p.b, p.i, p.gb, x, 0, apx, apx, 1.0f, lane);
+        }
+      } else if (rank == sm.draw_chunk) {
+        const float tl = sm.t_local;
+        if (cw == 0) {
+          const bool early = earlier_rejection(P, p.b, p.i, lane);
+          if (lane == 0) sm.skip = early;
+        }
+        named_bar_sync(kConsumerBar, kCT);
+        if (sm.skip) {               // a rejection earlier in the row: this draw is never emitted
+          if (cw == 0) finish_position(P, p.b, p.i, p.gb, -1, 0, apx, apx, 1.0f, lane);
+          named_bar_sync(kConsumerBar, kCT);   // sm.skip is read before it is reused
+          continue;
+        }
+        fill_p_sums(rowt, kk, cb, x);
+        named_bar_sync(kConsumerBar, kCT);
+        int finisher = 0;
+        const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm, ctid,
+                                         finisher, x);
+        if (cw == finisher)
+          finish_position(P, p.b, p.i, p.gb, tok, tok < 0 ? kFlagBad : 0, apx, apx, 1.0f, lane);
+      }
+      continue;
+    }
+
     if (kind == kBonus) {
       // Bonus token from p at position gamma_b ([R] One round, step 5).
       const int dch = cbad ? -1 : sm.draw_chunk;
@@ -849,7 +941,7 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
           if (cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagAccept, 0.0f, 0.0f, 0.0f, lane);
           continue;
         }
-        fill_p_sums(rowt, kk, cb);
+        fill_p_sums(rowt, kk, cb, -1);
         named_bar_sync(kConsumerBar, kCT);
         int finisher = 0;
         const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm, ctid,

@@ -103,11 +103,12 @@ class Workload:
         """Verified positions: sum over rows of (gamma_b + 1)."""
         return int(np.sum(self.draft_len.astype(np.int64) + 1))
 
-    def algorithmic_bytes(self) -> int:
+    def algorithmic_bytes(self, onehot: bool = False) -> int:
         """Logit bytes the method must read once: (2 gamma_b + 1) rows for a sampled row, gamma_b + 1
-        target rows for a greedy row, plus the per-row scalars, tokens, uniforms and outputs."""
+        target rows for a greedy row (and for every row when the drafts are one-hot: no draft
+        logits exist), plus the per-row scalars, tokens, uniforms and outputs."""
         g = self.draft_len.astype(np.int64)
-        greedy = self.temperature == 0
+        greedy = (self.temperature == 0) | onehot
         rows = np.where(greedy, g + 1, 2 * g + 1)
         logit = int(np.sum(rows)) * self.V * self.elem_bytes
         G = self.G
