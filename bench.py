@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--onehot", action="store_true",
                     help="one-hot drafts (greedy drafter): time spec_verify_onehot, no draft logits")
+    ap.add_argument("--tree", action="store_true",
+                    help="greedy tree verification: Medusa-shaped trees (top 2 of 4 heads, 31 nodes), "
+                         "B=256, V=128256 bf16, timed through spec_verify_tree_greedy")
     return ap.parse_args()
 
 
@@ -185,12 +188,41 @@ def oracle_sample_rate(cfg_key, seconds, onehot=False):
     return pos / secs, w.B, pos, secs
 
 
+def run_reference_tree(args):
+    """The oracle arm of --tree: oracle_tree_greedy on 16 host-drawn trees per step."""
+    from oracle.spec_verify_oracle import oracle_tree_greedy
+    hz, ht, hp = tree_inputs(16, 99, "numpy")
+    N = hz.shape[1]
+    for _ in range(args.warmup):
+        oracle_tree_greedy(hz, ht, hp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_tree_greedy(hz, ht, hp)
+    total = time.perf_counter() - t0
+    value = 16 * N * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"tree_greedy_b{TREE_B}_n{N}_v{TREE_V}_bf16", "sample_trees_per_step": 16},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "16 trees of the workload drawn on the host per step, single-thread "
+                                   "fp64 oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ.setdefault(v, "1")
+    if args.tree:
+        return run_reference_tree(args)
     from workloads import get_config
     cfg = get_config(args.workload)
     per_step = 1.5      # seconds of single-thread oracle work per step
@@ -374,10 +406,176 @@ def run_gpu(args):
     return 0
 
 
+# ------------------------------------------------------------------------------------------------
+# Tree verification (--tree)
+# ------------------------------------------------------------------------------------------------
+
+TREE_B, TREE_TOPK, TREE_HEADS, TREE_V = 256, 2, 4, 128256
+
+
+def tree_parents():
+    """The page's Medusa tree: the root, then the top-k candidates of each head under every node of
+    the previous level (parents before children)."""
+    import numpy as np
+    parents, level = [-1], [0]
+    for _ in range(TREE_HEADS):
+        new = []
+        for par in level:
+            for _ in range(TREE_TOPK):
+                new.append(len(parents))
+                parents.append(par)
+        level = new
+    return np.array(parents, np.int32)
+
+
+def tree_inputs(B, seed, backend):
+    """Target logits at every node (N(0, 2.5^2) plus the Zipf bias of the V=128256 workload) and node
+    tokens that equal the target's argmax at their parent with probability 0.7 (else uniform)."""
+    import numpy as np
+    par = tree_parents()
+    N = len(par)
+    if backend == "numpy":
+        rng = np.random.default_rng(seed)
+        bias = -1.1 * np.log1p(rng.permutation(TREE_V)).astype(np.float32)
+        zt = (rng.standard_normal((B, N, TREE_V), dtype=np.float32) * 2.5 + bias)
+        from workloads import bf16_round
+        zt = bf16_round(zt)
+        g = zt.argmax(-1)
+        tok = np.where(rng.random((B, N)) < 0.7, g[:, np.maximum(par, 0)],
+                       rng.integers(0, TREE_V, (B, N))).astype(np.int32)
+        return zt, tok, np.tile(par, (B, 1))
+    import torch
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    bias = -1.1 * torch.log1p(torch.randperm(TREE_V, device="cuda", generator=gen).float())
+    zt = (torch.randn((B, N, TREE_V), device="cuda", generator=gen) * 2.5 + bias).to(torch.bfloat16)
+    g = zt.float().argmax(-1)
+    pidx = torch.from_numpy(np.maximum(par, 0)).cuda().long()
+    rnd = torch.randint(0, TREE_V, (B, N), device="cuda", generator=gen)
+    keep = torch.rand((B, N), device="cuda", generator=gen) < 0.7
+    tok = torch.where(keep, g[:, pidx], rnd).to(torch.int32).contiguous()
+    return zt, tok, torch.from_numpy(np.tile(par, (B, 1))).cuda()
+
+
+def run_tree(args):
+    import numpy as np
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import speculative_decoding_verification_55_gb300 as sv
+    sv.build_library()
+    B = min(args.rows, TREE_B) if args.rows else TREE_B
+    zt, tok, par = tree_inputs(B, 7 + 1000 * rank, "torch")
+    N = zt.shape[1]
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.workspace_for(B, N - 1, TREE_V, sv.SV_DTYPE_BF16, dev, stream)
+    outs = [torch.empty((B, N), dtype=torch.int32, device=dev), torch.empty((B,), dtype=torch.int32, device=dev),
+            torch.empty((B, N + 1), dtype=torch.int32, device=dev), torch.empty((B, N), dtype=torch.int32, device=dev)]
+
+    def call(z, t, p):
+        sv.spec_verify_tree_greedy(z, t, p, None, outs[0], outs[1], outs[2], outs[3], ws, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        call(zt, tok, par)
+    torch.cuda.synchronize(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        call(zt, tok, par)
+    ev1.record(stream)
+    barrier()
+    ms_step = ev0.elapsed_time(ev1) / args.steps
+    clock_info = clocks.stop()
+    if world > 1:
+        mt = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(mt.item())
+    nodes = B * N
+    algo = B * N * TREE_V * 2 + B * N * 8 + B * (N + N + 1 + N + 1) * 4
+    achieved = algo / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    e2e = None
+    if not args.no_e2e:
+        host = [x.cpu().pin_memory() for x in (zt, tok, par)]
+        dev_in = [torch.empty_like(x) for x in (zt, tok, par)]
+        h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in outs]
+        bi = sum(x.numel() * x.element_size() for x in host)
+        bo = sum(x.numel() * x.element_size() for x in h_out)
+
+        def e2e_step():
+            for d_, h_ in zip(dev_in, host):
+                d_.copy_(h_, non_blocking=True)
+            call(*dev_in)
+            for h_, o_ in zip(h_out, outs):
+                h_.copy_(o_, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ms_e2e = e0.elapsed_time(e1) / n_e2e
+        e2e = {"value": nodes * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+               "d2h_bytes_per_step": int(bo), "ms_per_step": ms_e2e, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        from oracle.spec_verify_oracle import oracle_tree_greedy
+        hz, ht, hp = tree_inputs(16, 99, "numpy")
+        t0 = time.perf_counter()
+        oracle_tree_greedy(hz, ht, hp)
+        secs = time.perf_counter() - t0
+        cpu = {"value": 16 * N / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"16 trees of the workload drawn on the host, {secs:.1f} s of single-thread "
+                         f"fp64 oracle work"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": nodes * world / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"tree_greedy_b{B}_n{N}_v{TREE_V}_bf16", "B": B, "nodes": N,
+                       "V": TREE_V, "tree": f"top {TREE_TOPK} of {TREE_HEADS} heads",
+                       "positions_per_gpu": nodes, "algorithmic_bytes_per_step": algo,
+                       "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+            "gpu_launches": args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind,
+                         "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "traffic": None,
+                         "kernel": "sv_stream_kernel<bf16>"},
+            "clocks": clock_info, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.tree:
+        return run_tree(args)
     return run_gpu(args)
 
 

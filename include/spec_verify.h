@@ -142,6 +142,35 @@ int spec_verify_onehot(const void* target_logits, const int32_t* draft_tokens,
                        int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                        void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* Greedy verification of a tree of candidates (Medusa-style drafts): [B] "Inference: distillation
+ * and speculative decoding", brunomaga.github.io -- Medusa (candidate continuations form a tree that
+ * the target verifies in one pass with tree attention; the longest accepted path is kept).
+ * Row b holds tree_size[b] nodes; node 0 is the root, the target's own next token, always kept.
+ * A node j > 0 is accepted when its parent is accepted and tree_tokens[b,j] equals the target's
+ * argmax at the parent (lowest index on ties). The path kept is the longest accepted one (the
+ * lowest node index among the deepest), and the target's argmax at its last node is the next token.
+ *
+ * target_logits  [B, N, V] dtype   the target's logits at every node (rows j >= tree_size never read)
+ * tree_tokens    [B, N]    int32   token of each node
+ * tree_parents   [B, N]    int32   parent of each node: -1 at the root, 0 <= parent < j otherwise
+ * tree_size      [B]       int32   nodes per row in [1, N]; NULL means N
+ * out_path       [B, N]    int32   node indices of the kept path, root first, then -1
+ * out_path_len   [B]       int32   nodes on the kept path (>= 1); -1 marks a row error
+ * out_tokens     [B, N+1]  int32   tokens of the path's nodes, then the next token, then -1
+ * out_pred       [B, N]    int32   the target's argmax at every node, -1 beyond tree_size (may be NULL)
+ * B, N, V, dtype                   1 <= N <= SV_MAX_GAMMA + 1; dtype as in spec_verify
+ * workspace                        as in spec_verify, sized spec_verify_workspace_size(B, N - 1, V,
+ *                                  dtype)
+ * Row errors (the row's outputs all -1): tree_size outside [1, N]; tree_parents[b,0] != -1 or a parent
+ * outside [0, j); a node token outside [0, V); a node's logit row with NaN or +inf, or only -inf.
+ * Only rows of 16-byte multiples with a 16-byte aligned target_logits are supported (other V:
+ * SV_ERR_BAD_SHAPE; a misaligned base: SV_ERR_MISALIGNED). Other argument errors as in spec_verify. */
+int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_tokens,
+                            const int32_t* tree_parents, const int32_t* tree_size,
+                            int32_t* out_path, int32_t* out_path_len, int32_t* out_tokens,
+                            int32_t* out_pred, int32_t B, int32_t N, int32_t V, int32_t dtype,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream);
+
 /* spec_verify_ex for callers that cannot allocate device memory. The pages have no counterpart:
  * this is a deployment convenience, not part of the method.
  *

@@ -22,6 +22,8 @@ What it computes, and where the pages define it (page title, then section):
   the accept probability and the normalised residual.
 * One-hot drafts ([B] Draft-model speculative decoding, the greedy-drafter special case):
   ``oracle_verify_onehot`` is the same verification with q_i = [v == x_i].
+* Greedy tree verification ([B] Medusa: a tree of candidates, the longest accepted path):
+  ``oracle_tree_greedy``.
 
 Parity status: every function below is pinned by the tests in ``tests/test_oracle.py`` and
 ``tests/test_montecarlo.py`` (page-printed worked examples, closed forms, identities, an exact
@@ -353,6 +355,82 @@ def oracle_verify_onehot(target_logits, draft_tokens, draft_len, temperature, un
             out_p[b] = r.p_draft
             out_q[b] = r.q_draft
     return BatchResult(out_tokens, out_num, out_alpha, out_p, out_q, results)
+
+
+# ----------------------------------------------------------------------------------------------
+# Greedy tree verification (Medusa-style candidate trees)
+# ----------------------------------------------------------------------------------------------
+
+@dataclass
+class TreeResult:
+    path: np.ndarray        # [B, N] node indices of the longest accepted path, root first, -1 padding
+    path_len: np.ndarray    # [B] nodes on the path (>= 1), -1 on a row error
+    tokens: np.ndarray      # [B, N+1] tokens of the path nodes, then the target's next token, -1 padding
+    pred: np.ndarray        # [B, N] target argmax at every node (-1 beyond the row's nodes or on error)
+
+
+def tree_row_is_valid(zt, tok, par, n, N, V):
+    """Row errors of a tree row: size outside [1, N]; the root's parent not -1; a parent outside
+    [0, node) for any other node; a node token outside [0, V); a node's logit row with NaN or +inf,
+    or only -inf."""
+    if not (1 <= n <= N):
+        return False
+    if int(par[0]) != -1:
+        return False
+    for i in range(1, n):
+        if not (0 <= int(par[i]) < i):
+            return False
+    for i in range(n):
+        if not (0 <= int(tok[i]) < V):
+            return False
+        if _bad_logits(zt[i]):
+            return False
+    return True
+
+
+def oracle_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size=None):
+    """Greedy verification of a tree of candidates, one row at a time ([B] "Inference: distillation
+    and speculative decoding" -- Medusa: the candidates form a tree verified in one target pass; the
+    root is the target's own next token; a node is accepted when its parent is accepted and its
+    token equals the target's argmax after its parent; the longest accepted path is kept, and the
+    target's argmax after the path's last node is the next token).
+
+    target_logits [B, N, V] (the target's logits at every node), tree_tokens [B, N], tree_parents
+    [B, N] (-1 at the root, parents before children), tree_size [B] or None (all N). Argmax ties go
+    to the lowest index; among the deepest accepted nodes the lowest node index ends the path."""
+    target_logits = np.asarray(target_logits)
+    B, N, V = target_logits.shape
+    if tree_size is None:
+        tree_size = np.full(B, N, dtype=np.int64)
+    path = np.full((B, N), -1, dtype=np.int32)
+    plen = np.full(B, -1, dtype=np.int32)
+    toks = np.full((B, N + 1), -1, dtype=np.int32)
+    pred = np.full((B, N), -1, dtype=np.int32)
+    for b in range(B):
+        n = int(tree_size[b])
+        tok, par = tree_tokens[b], tree_parents[b]
+        if not tree_row_is_valid(target_logits[b], tok, par, n, N, V):
+            continue
+        g = [greedy_argmax(target_logits[b, i]) for i in range(n)]
+        accepted = {0: 1}                 # node -> nodes on its path from the root
+        best = 0
+        for i in range(1, n):
+            pi = int(par[i])
+            if pi in accepted and int(tok[i]) == g[pi]:
+                accepted[i] = accepted[pi] + 1
+                if accepted[i] > accepted[best]:
+                    best = i
+        nodes = [best]
+        while nodes[-1] != 0:
+            nodes.append(int(par[nodes[-1]]))
+        nodes.reverse()
+        L = len(nodes)
+        path[b, :L] = nodes
+        plen[b] = L
+        toks[b, :L] = [int(tok[j]) for j in nodes]
+        toks[b, L] = g[best]
+        pred[b, :n] = g
+    return TreeResult(path, plen, toks, pred)
 
 
 # ----------------------------------------------------------------------------------------------

@@ -25,7 +25,7 @@ SV_ERR_SCRATCH_TOO_SMALL = 8
 SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_onehot",
-            "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
+            "spec_verify_tree_greedy", "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
             "spec_verify_version")
 
 _lib = None
@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_noalloc.restype = ctypes.c_int
             L.spec_verify_onehot.argtypes = [vp, i32p, i32p, f32p, f32p, i32p, i32p, f32p, f32p, f32p] + tail
             L.spec_verify_onehot.restype = ctypes.c_int
+            L.spec_verify_tree_greedy.argtypes = [vp, i32p, i32p, i32p, i32p, i32p, i32p, i32p] + tail
+            L.spec_verify_tree_greedy.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
             L.spec_verify_workspace_size.restype = ctypes.c_size_t
             L.spec_verify_workspace_status.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int32), vp]
@@ -221,6 +223,47 @@ def spec_verify_onehot(target_logits, draft_tokens, draft_len, temperature, unif
         _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_onehot")
+
+
+def spec_verify_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size, out_path,
+                            out_path_len, out_tokens, out_pred, workspace, stream=None) -> None:
+    """Calls the C ABI spec_verify_tree_greedy (greedy verification of candidate trees) on torch
+    tensors: target_logits [B, N, V]. Raises SpecVerifyError on a nonzero status."""
+    import torch
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    _check(target_logits, "target_logits", device=dev)
+    _check(tree_tokens, "tree_tokens", torch.int32, (B, N), dev)
+    _check(tree_parents, "tree_parents", torch.int32, (B, N), dev)
+    _check(tree_size, "tree_size", torch.int32, (B,), dev)
+    _check(out_path, "out_path", torch.int32, (B, N), dev)
+    _check(out_path_len, "out_path_len", torch.int32, (B,), dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B, N + 1), dev)
+    _check(out_pred, "out_pred", torch.int32, (B, N), dev)
+    _check(workspace, "workspace", device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().spec_verify_tree_greedy(
+        _ptr(target_logits), _ptr(tree_tokens), _ptr(tree_parents), _ptr(tree_size),
+        _ptr(out_path), _ptr(out_path_len), _ptr(out_tokens), _ptr(out_pred), B, N, V,
+        _dtype_code(target_logits), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_tree_greedy")
+
+
+def verify_tree(target_logits, tree_tokens, tree_parents, tree_size=None, stream=None):
+    """Allocates the outputs, runs spec_verify_tree_greedy and returns
+    (out_path [B, N], out_path_len [B], out_tokens [B, N+1], out_pred [B, N])."""
+    import torch
+    B, N, V = target_logits.shape
+    dev = target_logits.device
+    out_path = torch.empty((B, N), dtype=torch.int32, device=dev)
+    out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    out_tokens = torch.empty((B, N + 1), dtype=torch.int32, device=dev)
+    out_pred = torch.empty((B, N), dtype=torch.int32, device=dev)
+    ws = workspace_for(B, N - 1, V, _dtype_code(target_logits), dev, stream)
+    spec_verify_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size, out_path, out_len,
+                            out_tokens, out_pred, ws, stream)
+    return out_path, out_len, out_tokens, out_pred
 
 
 def spec_verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,

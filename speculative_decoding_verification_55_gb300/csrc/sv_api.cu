@@ -240,6 +240,65 @@ int spec_verify_ex(const void* target_logits, const void* draft_logits, const in
                      V, dtype, workspace, workspace_bytes, cuda_stream, false);
 }
 
+int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_tokens,
+                            const int32_t* tree_parents, const int32_t* tree_size,
+                            int32_t* out_path, int32_t* out_path_len, int32_t* out_tokens,
+                            int32_t* out_pred, int32_t B, int32_t N, int32_t V, int32_t dtype,
+                            void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
+  if (N < 1 || !sizes_ok(B, N - 1, V, dtype)) return SV_ERR_BAD_SHAPE;
+  if (!target_logits || !tree_tokens || !tree_parents || !out_path || !out_path_len || !out_tokens)
+    return SV_ERR_NULL_POINTER;
+  const bool bf16 = dtype == SV_DTYPE_BF16;
+  const uintptr_t es = bf16 ? 2 : 4;
+  auto mis = [](const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; };
+  if (mis(target_logits, es) || mis(tree_tokens, 4) || mis(tree_parents, 4) || mis(tree_size, 4) ||
+      mis(out_path, 4) || mis(out_path_len, 4) || mis(out_tokens, 4) || mis(out_pred, 4) ||
+      mis(workspace, 16))
+    return SV_ERR_MISALIGNED;
+  const int G = N - 1;
+  const size_t need = spec_verify_workspace_size(B, G, V, dtype);
+  if (!workspace || workspace_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
+  if (static_cast<long long>(B) * N > INT_MAX / sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
+  // Tree rows run on the streaming kernel only (rows of 16-byte multiples, 16-byte aligned base).
+  if ((static_cast<size_t>(V) * es) % 16 != 0) return SV_ERR_BAD_SHAPE;
+  if (reinterpret_cast<uintptr_t>(target_logits) % 16 != 0) return SV_ERR_MISALIGNED;
+  const int sC = stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es));
+  if (sC == 0) return SV_ERR_BAD_SHAPE;
+  int dev = 0;
+  const int dev_status = check_device(&dev);
+  if (dev_status != SV_OK) return dev_status;
+
+  sv::Params P{};
+  P.tree = 1;
+  P.zt = target_logits;
+  P.ttok = tree_tokens;
+  P.tparent = tree_parents;
+  P.tsize = tree_size;
+  P.out_path = out_path;
+  P.out_plen = out_path_len;
+  P.out_tokens = out_tokens;
+  P.out_pred = out_pred;
+  char* ws = static_cast<char*>(workspace);
+  P.rec = reinterpret_cast<int2*>(ws);
+  P.cnt = reinterpret_cast<unsigned*>(ws + records_bytes(B, G));
+  P.status = P.cnt + B;
+  P.B = B;
+  P.G = G;
+  P.V = V;
+  const int E = static_cast<int>(16 / es);
+  P.units = V / E;
+  P.C = sC;
+  P.per = (P.units + P.C - 1) / P.C;
+  int maxc = 0;
+  if (max_clusters(dev, bf16, P.C, &maxc) != SV_OK) return SV_ERR_CUDA;
+  const long long slots = static_cast<long long>(B) * N;
+  P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
+  if (sv::launch_stream(P, bf16, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 int spec_verify_onehot(const void* target_logits, const int32_t* draft_tokens,
                        const int32_t* draft_len, const float* temperature, const float* uniforms,
                        int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,

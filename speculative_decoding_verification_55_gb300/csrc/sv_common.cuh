@@ -50,7 +50,17 @@ struct Params {
   int per;                   // units per CTA chunk
   int nclusters;             // clusters in the grid (persistent kernel)
   int onehot;                // drafted positions have one-hot drafts q = [v == x] (no draft logits)
+  // Greedy tree verification (tree != 0): positions are the N = G + 1 tree nodes of each row.
+  int tree;
+  const int32_t* tparent;    // [B, N] parent of each node, -1 at the root
+  const int32_t* ttok;       // [B, N] token of each node
+  const int32_t* tsize;      // [B] nodes per row, or null (N)
+  int32_t* out_path;         // [B, N] longest accepted path, root first
+  int32_t* out_plen;         // [B] nodes on the path
+  int32_t* out_pred;         // [B, N] target argmax per node, or null
 };
+
+constexpr int kMaxTreeNodes = 65;    // N <= SV_MAX_GAMMA + 1
 
 // ------------------------------------------------------------------------------------------------
 // Arithmetic
@@ -510,6 +520,88 @@ __device__ __forceinline__ void finish_position(const Params& P, int b, int i, i
     P.out_num[b] = err ? -1 : kk + 1;
     P.cnt[b] = 0u;                                     // leave the workspace zeroed
   }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Greedy tree verification: the row's outputs when the tree itself is invalid, and the finish of
+// one node (its argmax recorded, then, for the row's last node, the walk of the tree).
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void write_tree_row_error(const Params& P, int b, int lane) {
+  const int N = P.G + 1;
+  for (int j = lane; j < N; j += 32) {
+    P.out_path[(size_t)b * N + j] = -1;
+    if (P.out_pred) P.out_pred[(size_t)b * N + j] = -1;
+  }
+  for (int j = lane; j <= N; j += 32) P.out_tokens[(size_t)b * (N + 1) + j] = -1;
+  if (lane == 0) P.out_plen[b] = -1;
+}
+
+// [B] "Inference: distillation and speculative decoding" -- Medusa: the root (node 0) is the
+// target's own next token; a node is accepted when its parent is accepted and its token equals the
+// target's argmax at the parent; the longest accepted path is kept (the lowest node index among
+// the deepest), and the target's argmax at its last node is the next token. `scr` is 2 *
+// kMaxTreeNodes ints of the calling warp's shared memory. One full warp.
+__device__ __forceinline__ void finish_tree_node(const Params& P, int b, int i, int nb, int cand,
+                                                 int bad, int* scr, int lane) {
+  const int N = P.G + 1;
+  unsigned old = 0;
+  __syncwarp();
+  if (lane == 0) {
+    P.rec[(size_t)b * N + i] = make_int2(cand, (bad ? kFlagBad : 0) | kFlagDone);
+    __threadfence();
+    old = atomicAdd(P.cnt + b, 1u);
+  }
+  old = __shfl_sync(kFull, old, 0);
+  if (old != static_cast<unsigned>(nb - 1)) return;
+  __threadfence();
+  int* pred = scr;                    // target argmax per node
+  int* len = scr + kMaxTreeNodes;     // nodes on the accepted path ending at a node, 0 if rejected
+  bool err = false;
+  for (int j = lane; j < nb; j += 32) {
+    const int2 r = __ldcg(P.rec + (size_t)b * N + j);
+    pred[j] = r.x;
+    const int t = __ldg(P.ttok + (size_t)b * N + j);
+    const int pa = __ldg(P.tparent + (size_t)b * N + j);
+    err |= (r.y & kFlagBad) || t < 0 || t >= P.V || (j == 0 ? pa != -1 : (pa < 0 || pa >= j));
+  }
+  err = __any_sync(kFull, err);
+  for (int j = lane; j < nb; j += 32) P.rec[(size_t)b * N + j] = make_int2(0, 0);   // leave zeros
+  __syncwarp();
+  int best = 0, blen = 1;
+  if (lane == 0 && !err) {
+    len[0] = 1;
+    for (int j = 1; j < nb; ++j) {
+      const int pa = __ldg(P.tparent + (size_t)b * N + j);
+      const int t = __ldg(P.ttok + (size_t)b * N + j);
+      len[j] = (len[pa] > 0 && t == pred[pa]) ? len[pa] + 1 : 0;
+      if (len[j] > blen) {
+        best = j;
+        blen = len[j];
+      }
+    }
+  }
+  __syncwarp();
+  best = __shfl_sync(kFull, best, 0);
+  blen = __shfl_sync(kFull, blen, 0);
+  if (err) {
+    write_tree_row_error(P, b, lane);
+  } else {
+    if (lane == 0) {
+      int node = best;
+      for (int d = blen - 1; d >= 0; --d) {     // root first: fill from the end of the path
+        P.out_path[(size_t)b * N + d] = node;
+        P.out_tokens[(size_t)b * (N + 1) + d] = __ldg(P.ttok + (size_t)b * N + node);
+        node = d > 0 ? __ldg(P.tparent + (size_t)b * N + node) : node;
+      }
+      P.out_tokens[(size_t)b * (N + 1) + blen] = pred[best];
+      P.out_plen[b] = blen;
+    }
+    for (int j = blen + lane; j < N; j += 32) P.out_path[(size_t)b * N + j] = -1;
+    for (int j = blen + 1 + lane; j <= N; j += 32) P.out_tokens[(size_t)b * (N + 1) + j] = -1;
+    if (P.out_pred)
+      for (int j = lane; j < N; j += 32) P.out_pred[(size_t)b * N + j] = j < nb ? pred[j] : -1;
+  }
+  if (lane == 0) P.cnt[b] = 0u;                  // leave the workspace zeroed
 }
 
 // Whether a position of row b before position i has already recorded a rejection (visible to this

@@ -107,6 +107,7 @@ struct Shared {
   float px, qx, t_local, p_tlocal;
   int acc, bad, cand, draw_chunk, p_chunk;
   int resid_mass;                    // one-hot drafts: p without x has positive mass
+  int tree_scr[2 * kMaxTreeNodes];   // the tree walk at a row's end (consumer warp 0)
   // ... and the pending drafted position whose residual totals this exchange carried
   float pend_alpha, pend_tlocal;
   int pend_chunk, pend_resid;
@@ -136,6 +137,15 @@ __device__ __forceinline__ Pos classify(const Params& P, int s) {
   Pos p;
   p.i = s / P.B;
   p.b = s - p.i * P.B;
+  if (P.tree) {                       // tree nodes: greedy positions 0 .. size-1 of the row
+    p.gb = (P.tsize ? __ldg(P.tsize + p.b) : P.G + 1) - 1;
+    p.T = 0.0f;
+    p.len_ok = p.gb >= 0 && p.gb <= P.G;
+    p.greedy = p.t_ok = true;
+    p.load = p.len_ok && p.i <= p.gb;
+    p.two = p.oh = false;
+    return p;
+  }
   p.gb = P.draft_len ? __ldg(P.draft_len + p.b) : P.G;
   p.T = __ldg(P.temperature + p.b);
   p.len_ok = p.gb >= 0 && p.gb <= P.G;
@@ -756,15 +766,19 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
   for (int s = cid; s < total; s += P.nclusters) {
     const Pos p = classify(P, s);
     if (!p.load) {
-      if (!(p.len_ok && p.t_ok) && p.i == 0 && rank == 0 && cw == 0) write_row_error(P, p.b, lane);
+      if (!(p.len_ok && p.t_ok) && p.i == 0 && rank == 0 && cw == 0) {
+        if (P.tree) write_tree_row_error(P, p.b, lane);
+        else write_row_error(P, p.b, lane);
+      }
       continue;
     }
-    const bool ok = row_scalars_ok(P, p.b, p.gb, p.greedy, lane);
+    // (tree rows: the tree's parents and tokens are checked by the walk at the row's end)
+    const bool ok = P.tree || row_scalars_ok(P, p.b, p.gb, p.greedy, lane);
     const int kind = p.greedy ? kArgmax : (p.two ? kVerify : (p.oh ? kOneHot : kBonus));
     const char* rowt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES;
     const char* rowd = p.two ? static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES
                              : nullptr;
-    const int x = p.i < p.gb ? __ldg(P.tokens + (size_t)p.b * G + p.i) : -1;
+    const int x = (!P.tree && p.i < p.gb) ? __ldg(P.tokens + (size_t)p.b * G + p.i) : -1;
 
     // Early scalar loads for the accept test (their latency hides behind pass 1).
     float zx_t = 0.0f, zx_d = 0.0f, u_acc = 0.0f, u_res = 0.0f, u_bon = 0.0f;
@@ -877,6 +891,10 @@ __global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_ke
     // the finishing work (records, counters, row emits) does not slow one rank down.
     const int fin = static_cast<int>((ex - 1) % static_cast<uint32_t>(C));
 
+    if (kind == kArgmax && P.tree) {
+      if (rank == fin && cw == 0) finish_tree_node(P, p.b, p.i, p.gb + 1, sm.cand, sm.bad, sm.tree_scr, lane);
+      continue;
+    }
     if (kind == kArgmax) {
       if (rank == fin && cw == 0) {
         const int acc = sm.acc;
