@@ -51,6 +51,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--onehot", action="store_true",
                     help="one-hot drafts (greedy drafter): time spec_verify_onehot, no draft logits")
+    ap.add_argument("--rollback", action="store_true",
+                    help="KV-cache rollback after a round: B=1024 rows of the default workload's draft "
+                         "lengths, 320 KB cache entries (80 layers of K and V, 8 heads x 128, bf16)")
     ap.add_argument("--tree", action="store_true",
                     help="greedy tree verification: Medusa-shaped trees (top 2 of 4 heads, 31 nodes), "
                          "B=256, V=128256 bf16, timed through spec_verify_tree_greedy")
@@ -570,12 +573,104 @@ def run_tree(args):
     return 0
 
 
+# ------------------------------------------------------------------------------------------------
+# KV-cache rollback (--rollback)
+# ------------------------------------------------------------------------------------------------
+
+RB_ENTRY = 80 * 2 * 8 * 128 * 2       # bytes of one token's cache entry: 80 layers of K and V
+RB_L = 16                              # entries per row: the prefix (2..6) plus gamma + 1 (<= 9)
+
+
+def rollback_inputs(seed):
+    """Row lengths of the default workload (gamma_b 1..8), prefixes of 2..6 entries, accept counts
+    drawn with alpha = 0.7 per position (k = first failure), 10% row errors."""
+    import numpy as np
+    from workloads import get_config
+    from workloads.generate import _row_params
+    cfg = get_config(DEFAULT_WORKLOAD)
+    rng = np.random.default_rng(seed)
+    g = np.asarray(_row_params(cfg, cfg.seed)[0])
+    B = len(g)
+    n = rng.integers(2, 7, B)
+    k = np.minimum(rng.geometric(0.3, B) - 1, g)
+    e = (k + 1).astype(np.int64)
+    e[rng.random(B) < 0.1] = -1
+    return n.astype(np.int32), g.astype(np.int32), e.astype(np.int32), (n + g).astype(np.int32)
+
+
+def run_rollback(args):
+    import numpy as np
+    import torch
+    from oracle.spec_verify_oracle import kv_rollback
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import speculative_decoding_verification_55_gb300 as sv
+    sv.build_library()
+    n, g, e, d = rollback_inputs(5)
+    B, G = len(n), int(g.max())
+    ti = lambda a: torch.as_tensor(a, device=dev)
+    n_t, g_t, e_t, d_t = ti(n), ti(g), ti(e), ti(d)
+    tl = torch.empty(B, dtype=torch.int32, device=dev)
+    dl = torch.empty(B, dtype=torch.int32, device=dev)
+    cache = torch.ones((B, RB_L, RB_ENTRY), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        sv.spec_verify_kv_rollback(n_t, g_t, e_t, d_t, tl, dl, cache=cache, gamma_max=G, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.steps):
+        flush.zero_()                  # the dropped entries are not in L2 when the step starts
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    clock_info = clocks.stop()
+    ms = float(np.median(times))
+    _, _, dropped = kv_rollback(n, g, e, d, G)
+    zero_bytes = sum(max(0, min(hi, RB_L) - max(lo, 0)) for lo, hi in dropped) * RB_ENTRY
+    algo = zero_bytes + B * 6 * 4
+    achieved = algo / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    want_t, want_d, _ = kv_rollback(n, g, e, d, G)
+    ok = np.array_equal(tl.cpu().numpy(), want_t) and np.array_equal(dl.cpu().numpy(), want_d)
+    line = {
+        "metric": "KV-cache rows rolled back per second and bytes zeroed (GB/s)", "value": B / (ms * 1e-3),
+        "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic",
+        "config": {"workload": f"kv_rollback_b{B}_entry{RB_ENTRY}", "B": B, "entries_per_row": RB_L,
+                   "entry_bytes": RB_ENTRY, "bytes_zeroed_per_step": zero_bytes,
+                   "algorithmic_bytes_per_step": algo, "l2": "256 MB written between steps",
+                   "lengths_match_oracle": ok},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "traffic": None,
+                     "kernel": "sv_rollback_kernel"},
+        "clocks": clock_info, "e2e": None, "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0 if ok else 1
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.tree:
         return run_tree(args)
+    if args.rollback:
+        return run_rollback(args)
     return run_gpu(args)
 
 

@@ -171,6 +171,32 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
                             int32_t* out_pred, int32_t B, int32_t N, int32_t V, int32_t dtype,
                             void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* KV-cache rollback after a verified round, batched over ragged rows. [R] "Speculative decoding",
+ * rayaq.ca ml-models -- Verification attention and the cache: the target's cache held n entries
+ * before the round and n + gamma + 1 after verification; with k drafts accepted the first n + k + 1
+ * are kept (the prefix, the last token, the accepted drafts) and the rest is dropped; the drafter's
+ * cache is rolled back the same way ([B] Draft-model speculative decoding: the drafter keeps the
+ * part of its cache that is still valid, which is one entry short on a full accept).
+ *
+ * prefix_len       [B] int32  n_b, target cache entries before the round
+ * draft_len        [B] int32  gamma_b (NULL: gamma_max); clamped to [0, gamma_max]
+ * out_num_emitted  [B] int32  k_b + 1 from spec_verify; -1 (a row error) commits nothing
+ * drafter_len_in   [B] int32  the drafter cache's entries now (NULL: taken as n_b + k_b + 1)
+ * target_len_out   [B] int32  n_b + k_b + 1 (n_b after a row error)
+ * drafter_len_out  [B] int32  min(drafter_len_in, target_len_out) (may be NULL)
+ * cache            optional contiguous target cache, row b at cache + b * cache_row_stride bytes,
+ *                  cache_entries entries of entry_bytes each; when not NULL the dropped entries
+ *                  [target_len_out, n_b + gamma_b + 1) of each row (clamped to cache_entries) are
+ *                  set to zero bytes. entry_bytes and cache_row_stride multiples of 16, cache 16-byte
+ *                  aligned (else SV_ERR_MISALIGNED); cache_row_stride >= entry_bytes * cache_entries.
+ * All pointers are device pointers owned by the caller; one launch on cuda_stream; argument errors
+ * return a status and launch nothing. */
+int spec_verify_kv_rollback(const int32_t* prefix_len, const int32_t* draft_len,
+                            const int32_t* out_num_emitted, const int32_t* drafter_len_in,
+                            int32_t* target_len_out, int32_t* drafter_len_out, void* cache,
+                            int64_t cache_row_stride, int32_t entry_bytes, int32_t cache_entries,
+                            int32_t B, int32_t gamma_max, void* cuda_stream);
+
 /* spec_verify_ex for callers that cannot allocate device memory. The pages have no counterpart:
  * this is a deployment convenience, not part of the method.
  *

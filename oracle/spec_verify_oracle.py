@@ -24,6 +24,7 @@ What it computes, and where the pages define it (page title, then section):
   ``oracle_verify_onehot`` is the same verification with q_i = [v == x_i].
 * Greedy tree verification ([B] Medusa: a tree of candidates, the longest accepted path):
   ``oracle_tree_greedy``.
+* The cache after a round ([R] Verification attention and the cache): ``kv_rollback``.
 
 Parity status: every function below is pinned by the tests in ``tests/test_oracle.py`` and
 ``tests/test_montecarlo.py`` (page-printed worked examples, closed forms, identities, an exact
@@ -431,6 +432,33 @@ def oracle_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size=None)
         toks[b, L] = g[best]
         pred[b, :n] = g
     return TreeResult(path, plen, toks, pred)
+
+
+# ----------------------------------------------------------------------------------------------
+# KV-cache rollback after a round
+# ----------------------------------------------------------------------------------------------
+
+def kv_rollback(prefix_len, draft_len, num_emitted, drafter_len, G):
+    """New cache lengths after a verified round, one row at a time ([R] Verification attention and
+    the cache: keep the first n + k + 1 entries of the target's cache, the prefix, the last token
+    and the accepted drafts; the drafter's cache is rolled back the same way, never beyond what it
+    holds). Returns (target_len, drafter_len, dropped) with dropped[b] = (first, end) entries of the
+    target cache that the round wrote and no longer keeps (end = n + gamma_b + 1). A row error
+    (num_emitted < 1) commits nothing."""
+    B = len(prefix_len)
+    target = np.zeros(B, dtype=np.int64)
+    drafter = np.zeros(B, dtype=np.int64)
+    dropped = []
+    for b in range(B):
+        n = int(prefix_len[b])
+        g = G if draft_len is None else min(max(int(draft_len[b]), 0), G)
+        e = int(num_emitted[b])
+        keep = n + e if e >= 1 else n          # e = k + 1
+        target[b] = keep
+        d = keep if drafter_len is None else int(drafter_len[b])
+        drafter[b] = min(d, keep)
+        dropped.append((keep, n + g + 1))
+    return target, drafter, dropped
 
 
 # ----------------------------------------------------------------------------------------------

@@ -25,7 +25,7 @@ SV_ERR_SCRATCH_TOO_SMALL = 8
 SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_onehot",
-            "spec_verify_tree_greedy", "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
+            "spec_verify_tree_greedy", "spec_verify_kv_rollback", "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
             "spec_verify_version")
 
 _lib = None
@@ -62,6 +62,9 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_onehot.restype = ctypes.c_int
             L.spec_verify_tree_greedy.argtypes = [vp, i32p, i32p, i32p, i32p, i32p, i32p, i32p] + tail
             L.spec_verify_tree_greedy.restype = ctypes.c_int
+            L.spec_verify_kv_rollback.argtypes = [i32p, i32p, i32p, i32p, i32p, i32p, vp, ctypes.c_int64,
+                                                  i32, i32, i32, i32, vp]
+            L.spec_verify_kv_rollback.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
             L.spec_verify_workspace_size.restype = ctypes.c_size_t
             L.spec_verify_workspace_status.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int32), vp]
@@ -248,6 +251,33 @@ def spec_verify_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size,
         _dtype_code(target_logits), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_tree_greedy")
+
+
+def spec_verify_kv_rollback(prefix_len, draft_len, out_num_emitted, drafter_len_in, target_len_out,
+                            drafter_len_out, cache=None, gamma_max=None, stream=None) -> None:
+    """Calls the C ABI spec_verify_kv_rollback on torch tensors. cache: an optional [B, L, ...]
+    contiguous tensor whose trailing dimensions form one entry; its dropped entries are zeroed."""
+    import torch
+    B = prefix_len.shape[0]
+    dev = prefix_len.device
+    for name, t in (("prefix_len", prefix_len), ("draft_len", draft_len),
+                    ("out_num_emitted", out_num_emitted), ("drafter_len_in", drafter_len_in),
+                    ("target_len_out", target_len_out), ("drafter_len_out", drafter_len_out)):
+        _check(t, name, torch.int32, (B,), dev)
+    if gamma_max is None:
+        raise ValueError("gamma_max is required")
+    stride = entry = entries = 0
+    if cache is not None:
+        _check(cache, "cache", device=dev)
+        entries = cache.shape[1]
+        entry = cache[0, 0].numel() * cache.element_size()
+        stride = cache[0].numel() * cache.element_size()
+    st = lib().spec_verify_kv_rollback(
+        _ptr(prefix_len), _ptr(draft_len), _ptr(out_num_emitted), _ptr(drafter_len_in),
+        _ptr(target_len_out), _ptr(drafter_len_out), _ptr(cache), stride, entry, entries, B,
+        gamma_max, _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_kv_rollback")
 
 
 def verify_tree(target_logits, tree_tokens, tree_parents, tree_size=None, stream=None):
