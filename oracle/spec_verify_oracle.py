@@ -24,6 +24,8 @@ What it computes, and where the pages define it (page title, then section):
   ``oracle_verify_onehot`` is the same verification with q_i = [v == x_i].
 * Greedy tree verification ([B] Medusa: a tree of candidates, the longest accepted path):
   ``oracle_tree_greedy``.
+* Top-k / top-p filtering before the test ([R] Why the output is exactly the target's):
+  ``filtered_softmax`` and the ``top_k`` / ``top_p`` arguments of ``verify_row`` / ``oracle_verify``.
 * The cache after a round ([R] Verification attention and the cache): ``kv_rollback``.
 
 Parity status: every function below is pinned by the tests in ``tests/test_oracle.py`` and
@@ -71,6 +73,42 @@ def temperature_softmax(z, T):
     m = np.max(y)
     e = np.exp(y - m)
     return e / np.sum(e)
+
+
+def filtered_softmax(z, T, top_k=0, top_p=1.0):
+    """The distribution the rule is given after top-k and top-p filtering ([R] Why the output is
+    exactly the target's: temperature, top-p and any penalties are applied to p and q before the
+    test). In order: softmax(z / T); top-k keeps every token whose logit is not below the k-th
+    largest (ties at the boundary all kept; top_k <= 0 or >= V keeps all); top-p, on the renormalised
+    top-k distribution, keeps a token when the mass of the tokens with a strictly larger logit is
+    below top_p (so ties go together and the largest logit is always kept; top_p >= 1 keeps all);
+    the kept probabilities are renormalised. Returns (probabilities, top-p margin): the margin is the
+    distance from top_p to the nearest cumulative mass at a logit boundary (1.0 without top-p)."""
+    z = np.asarray(z, dtype=np.float64)
+    p = temperature_softmax(z, T)
+    V = z.shape[0]
+    keep = np.ones(V, dtype=bool)
+    if 0 < top_k < V:
+        kth = np.sort(z)[::-1][top_k - 1]
+        keep &= z >= kth
+    pk = np.where(keep, p, 0.0)
+    pk = pk / np.sum(pk)
+    margin = 1.0
+    if np.float64(top_p) < 1.0:
+        levels = np.unique(z[keep])[::-1]                 # distinct kept logits, largest first
+        above = 0.0
+        keep_p = np.zeros(V, dtype=bool)
+        margin = abs(np.float64(top_p))
+        for lv in levels:
+            grp = keep & (z == lv)
+            if above < np.float64(top_p):
+                keep_p |= grp
+            above += np.sum(pk[grp])
+            margin = min(margin, abs(above - np.float64(top_p)))
+        keep &= keep_p
+        pk = np.where(keep, pk, 0.0)
+        pk = pk / np.sum(pk)
+    return pk, margin
 
 
 def accept_ratio(p_x, q_x):
@@ -178,19 +216,24 @@ class RowResult:
     outcomes: dict = field(default_factory=dict)   # legit k -> admissible final tokens (diagnostics)
     exact: bool = True              # True when the only legit outcome is (k, tokens[-1])
     final_gap: float = 1.0
+    filter_margin: float = 1.0      # top-p: nearest cumulative boundary to top_p (1.0 without)
 
 
-def verify_row(zt, zd, x, gamma_b, T, u, G, diagnostics=False, eps=MARGIN):
+def verify_row(zt, zd, x, gamma_b, T, u, G, diagnostics=False, eps=MARGIN, top_k=0, top_p=1.0):
     """One row of the batch: the round's verification half ([R] One round steps 3-5 and
     Implementation, after the target pass; [R] The greedy case for T == 0).
 
     zt: [G+1, V] target logits, zd: [G, V] draft logits, x: [G] drafted tokens, u: [G+2] uniforms.
+    top_k, top_p: the row's filtering, applied to p and q alike (see filtered_softmax; sampled rows).
     """
     V = np.asarray(zt).shape[-1]
     alpha = np.zeros(G)
     pd = np.zeros(G)
     qd = np.zeros(G)
     if not row_is_valid(zt, zd, x, gamma_b, T, u, G, V):
+        return RowResult([], -1, alpha, pd, qd, valid=False)
+    if np.float64(T) != 0.0 and not np.float64(top_p) > 0.0:
+        # A nucleus of no mass keeps nothing: a sampled row asking for it has no distribution.
         return RowResult([], -1, alpha, pd, qd, valid=False)
 
     if np.float64(T) == 0.0:
@@ -213,9 +256,17 @@ def verify_row(zt, zd, x, gamma_b, T, u, G, diagnostics=False, eps=MARGIN):
     ratio = np.zeros(gamma_b)
     margin = np.zeros(gamma_b)
     p_rows, q_rows = [], []
+    fmargin = 1.0
+
+    def dist(z):
+        nonlocal fmargin
+        w, m = filtered_softmax(z, T, top_k, top_p)
+        fmargin = min(fmargin, m)
+        return w
+
     for i in range(gamma_b):
-        p = temperature_softmax(zt[i], T)
-        q = temperature_softmax(zd[i], T)
+        p = dist(zt[i])
+        q = dist(zd[i])
         p_rows.append(p)
         q_rows.append(q)
         xi = int(x[i])
@@ -237,14 +288,17 @@ def verify_row(zt, zd, x, gamma_b, T, u, G, diagnostics=False, eps=MARGIN):
             if not np.sum(w) > 0.0:                           # zero residual mass: draw from p
                 w = p_rows[kk]
         else:
-            w = temperature_softmax(zt[gamma_b], T)            # [R] One round, step 5 (bonus)
+            w = p_bonus                                        # [R] One round, step 5 (bonus)
             uu = np.float64(u[G + 1])
         return w, uu
+
+    p_bonus = dist(zt[gamma_b])
 
     w, uu = final_draw(k)
     j = inverse_cdf(w, uu)
     res = RowResult([int(x[i]) for i in range(k)] + [j], k, alpha, pd, qd,
                     ratio=ratio, margin=margin)
+    res.filter_margin = fmargin
     if diagnostics:
         # Every accept count reachable when decisions within eps of their threshold may go either way,
         # and for each the tokens whose CDF interval lies within eps of the draw's threshold.
@@ -278,7 +332,7 @@ class BatchResult:
 
 
 def oracle_verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
-                  rows=None, diagnostics=False, eps=MARGIN):
+                  rows=None, diagnostics=False, eps=MARGIN, top_k=None, top_p=None):
     """Batched verification, one row at a time in plain loops.
 
     target_logits [B, G+1, V], draft_logits [B, G, V] (any float dtype holding the stored values),
@@ -299,7 +353,9 @@ def oracle_verify(target_logits, draft_logits, draft_tokens, draft_len, temperat
     for b in (range(B) if rows is None else rows):
         zd = draft_logits[b] if draft_logits is not None else np.zeros((G, V))
         r = verify_row(target_logits[b], zd, draft_tokens[b], int(draft_len[b]),
-                       np.float32(temperature[b]), uniforms[b], G, diagnostics=diagnostics, eps=eps)
+                       np.float32(temperature[b]), uniforms[b], G, diagnostics=diagnostics, eps=eps,
+                       top_k=0 if top_k is None else int(top_k[b]),
+                       top_p=1.0 if top_p is None else np.float64(np.float32(top_p[b])))
         results[b] = r
         if r.valid:
             out_tokens[b, :len(r.tokens)] = r.tokens

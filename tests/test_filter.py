@@ -1,0 +1,190 @@
+"""Top-k / top-p filtering before the test: oracle pins on the CPU and GPU parity of
+spec_verify_filtered.
+
+[R] "Speculative decoding" (rayaq.ca), Why the output is exactly the target's: temperature, top-p
+and any penalties are applied to p and q before the test, because the rule keeps exactly the
+distribution it is given; [R] Pitfalls: a top-p that differs between p and q quietly breaks the
+identical-distribution guarantee, so both get the same filter. The pages name top-p without a
+formula; the reading pinned here is the usual one: top-k keeps the tokens whose logit is at least
+the k-th largest, top-p keeps a token when the mass of the strictly larger logits is below top_p,
+ties go together, the kept mass is renormalised.
+"""
+import numpy as np
+import pytest
+from scipy import special, stats
+
+from _parity import TOL, compare
+from oracle.spec_verify_oracle import (filtered_softmax, inverse_cdf, oracle_verify,
+                                       temperature_softmax)
+from workloads import bf16_round
+
+
+def softmax_T(z, T):
+    return special.softmax(np.asarray(z, np.float64) / np.float64(T))
+
+
+def rank_definition(z, k):
+    """Brute force: token v survives top-k when fewer than k tokens have a strictly larger logit."""
+    z = np.asarray(z, np.float64)
+    return np.array([np.sum(z > z[v]) < k for v in range(z.size)])
+
+
+def mass_definition(z, p, top_p):
+    """Brute force: token v survives top-p when the mass of the strictly larger logits is below
+    top_p (p already renormalised over the top-k set, zero outside it)."""
+    z = np.asarray(z, np.float64)
+    return np.array([p[v] > 0 and np.sum(p[z > z[v]]) < top_p for v in range(z.size)])
+
+
+# ------------------------------------------------------------------------------------------------
+# Oracle pins (CPU)
+# ------------------------------------------------------------------------------------------------
+
+def test_worked_example_by_hand():
+    """p = (0.5, 0.3, 0.15, 0.05): cumulative masses 0.5, 0.8, 0.95, 1.0. top_p = 0.79 keeps the
+    first two, renormalised to (0.625, 0.375); top_p = 0.81 also keeps the third (/0.95); top_k = 3
+    drops the last; top_k = 2 with top_p = 0.7 renormalises to (0.625, 0.375) first, where 0.625 <
+    0.7 still admits the second token."""
+    p = np.array([0.5, 0.3, 0.15, 0.05])
+    z = np.log(p)
+    w, m = filtered_softmax(z, 1.0, 0, 0.79)
+    assert np.allclose(w, [0.625, 0.375, 0.0, 0.0], atol=1e-15)
+    assert m == pytest.approx(0.01, abs=1e-12)
+    w, _ = filtered_softmax(z, 1.0, 0, 0.81)
+    assert np.allclose(w, [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95, 0.0], atol=1e-15)
+    w, m = filtered_softmax(z, 1.0, 3, 1.0)
+    assert np.allclose(w, [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95, 0.0], atol=1e-15)
+    assert m == 1.0
+    w, _ = filtered_softmax(z, 1.0, 2, 0.7)
+    assert np.allclose(w, [0.625, 0.375, 0.0, 0.0], atol=1e-15)
+    w, _ = filtered_softmax(z, 1.0, 2, 0.6)
+    assert np.allclose(w, [1.0, 0.0, 0.0, 0.0], atol=1e-15)
+
+
+def test_against_brute_force_definitions():
+    rng = np.random.default_rng(1)
+    for trial in range(400):
+        V = int(rng.integers(1, 30))
+        z = rng.standard_normal(V) * 2.0
+        if trial % 3 == 0:
+            z = np.round(z)                       # ties across the boundaries
+        if trial % 7 == 0:
+            z[rng.random(V) < 0.3] = -np.inf
+            z[0] = 0.5
+        T = float(rng.uniform(0.3, 2.0))
+        k = int(rng.integers(0, V + 2))
+        top_p = float(rng.choice([1.0, rng.uniform(0.01, 1.0)]))
+        w, _ = filtered_softmax(z, T, k, top_p)
+        p = softmax_T(z, T)
+        keep = rank_definition(z, k) if 0 < k < V else np.ones(V, bool)
+        pk = np.where(keep, p, 0.0)
+        pk /= pk.sum()
+        if top_p < 1.0:
+            keep &= mass_definition(z, pk, top_p)
+        want = np.where(keep, p, 0.0)
+        want /= want.sum()
+        assert np.allclose(w, want, rtol=1e-12, atol=1e-15), (z, T, k, top_p)
+        assert w.sum() == pytest.approx(1.0, abs=1e-12)
+
+
+def test_degenerate_settings():
+    rng = np.random.default_rng(2)
+    z = rng.standard_normal(50)
+    base = temperature_softmax(z, 0.8)
+    for k, tp in ((0, 1.0), (50, 1.0), (51, 1.0), (-3, 1.0), (0, 1.5)):
+        w, m = filtered_softmax(z, 0.8, k, tp)
+        assert np.array_equal(w, base) and m == 1.0
+    # top_k = 1 and a tiny top_p keep the argmax alone
+    for k, tp in ((1, 1.0), (0, 1e-9)):
+        w, _ = filtered_softmax(z, 0.8, k, tp)
+        assert np.array_equal(w, np.eye(50)[np.argmax(z)])
+    # all logits equal: every token ties with the k-th and with the top group, so all are kept
+    zz = np.full(9, 1.25)
+    for k, tp in ((3, 1.0), (0, 0.5), (1, 0.01)):
+        w, _ = filtered_softmax(zz, 1.0, k, tp)
+        assert np.allclose(w, np.full(9, 1 / 9), atol=1e-15)
+
+
+def test_margin_is_the_distance_to_the_nearest_boundary():
+    z = np.log(np.array([0.4, 0.4, 0.2]))       # groups: {0, 1} (0.8), {2} (0.2)
+    _, m = filtered_softmax(z, 1.0, 0, 0.75)
+    assert m == pytest.approx(0.05, abs=1e-12)   # |0.8 - 0.75|
+    _, m = filtered_softmax(z, 1.0, 0, 0.9)
+    assert m == pytest.approx(0.1, abs=1e-12)    # min(|0.8 - 0.9|, |1.0 - 0.9|)
+
+
+def test_filters_off_give_the_plain_rule():
+    rng = np.random.default_rng(3)
+    B, G, V = 6, 4, 40
+    zt = rng.standard_normal((B, G + 1, V)) * 2
+    zd = zt[:, :G] + rng.standard_normal((B, G, V))
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    T[0] = 0.0
+    u = rng.random((B, G + 2)).astype(np.float32)
+    a = oracle_verify(zt, zd, x, None, T, u)
+    o = oracle_verify(zt, zd, x, None, T, u, top_k=np.array([0, V, V + 3, -1, 0, V]),
+                      top_p=np.array([1.0, 1.0, 2.0, 1.0, 1.0, 1.0], np.float32))
+    for name in ("out_tokens", "out_num_emitted", "out_alpha", "out_p_draft", "out_q_draft"):
+        assert np.array_equal(getattr(a, name), getattr(o, name)), name
+
+
+def test_filtered_quantities():
+    """alpha = sum min(p~, q~), p~(x), q~(x) and the bonus drawn from the filtered target."""
+    rng = np.random.default_rng(4)
+    V = 30
+    zt = rng.standard_normal((1, 2, V)) * 2
+    zd = zt[:, :1] + rng.standard_normal((1, 1, V))
+    x = np.array([[int(np.argmax(zd[0, 0]))]], np.int32)
+    T = np.array([0.9], np.float32)
+    u = np.array([[0.0, 0.3, 0.77]], np.float32)        # u[0] = 0: the draft is kept
+    o = oracle_verify(zt, zd, x, None, T, u, top_k=np.array([7]), top_p=np.array([0.8], np.float32))
+    tp = np.float64(np.float32(0.8))
+    p, _ = filtered_softmax(zt[0, 0], T[0], 7, tp)
+    q, _ = filtered_softmax(zd[0, 0], T[0], 7, tp)
+    assert o.out_alpha[0, 0] == pytest.approx(np.minimum(p, q).sum(), abs=1e-14)
+    assert o.out_p_draft[0, 0] == pytest.approx(p[x[0, 0]], abs=1e-14)
+    assert o.out_q_draft[0, 0] == pytest.approx(q[x[0, 0]], abs=1e-14)
+    pb, _ = filtered_softmax(zt[0, 1], T[0], 7, tp)
+    assert o.out_num_emitted[0] == 2
+    assert o.out_tokens[0, 1] == inverse_cdf(pb, np.float64(u[0, 2]))
+    assert pb[o.out_tokens[0, 1]] > 0
+
+
+@pytest.mark.parametrize("top_p", [0.0, -0.5, np.nan])
+def test_row_error_for_an_empty_nucleus(top_p):
+    rng = np.random.default_rng(5)
+    B, G, V = 3, 2, 12
+    zt = rng.standard_normal((B, G + 1, V))
+    zd = rng.standard_normal((B, G, V))
+    x = rng.integers(0, V, (B, G)).astype(np.int32)
+    T = np.array([1.0, 0.0, 1.0], np.float32)            # row 1 greedy: filtering does not apply
+    u = rng.random((B, G + 2)).astype(np.float32)
+    o = oracle_verify(zt, zd, x, None, T, u, top_p=np.array([top_p, top_p, 1.0], np.float32))
+    assert o.out_num_emitted[0] == -1 and (o.out_tokens[0] == -1).all()
+    assert o.out_num_emitted[1] >= 1 and o.out_num_emitted[2] >= 1
+
+
+def test_emitted_token_follows_the_filtered_target():
+    """Monte Carlo of the page's guarantee for filtered distributions: drafts drawn from q~, the
+    first emitted token follows p~ (chi-square, fixed seed), and nothing outside p~'s support is
+    ever emitted."""
+    pt = np.array([0.30, 0.25, 0.2, 0.1, 0.08, 0.07])
+    pd = np.array([0.1, 0.4, 0.05, 0.3, 0.1, 0.05])
+    zt = np.log(pt)[None, None, :].repeat(2, axis=1)
+    zd = np.log(pd)[None, None, :]
+    k, top_p = 4, np.float32(0.8)
+    want, _ = filtered_softmax(zt[0, 0], 1.0, k, np.float64(top_p))
+    q, _ = filtered_softmax(zd[0, 0], 1.0, k, np.float64(top_p))
+    rng = np.random.default_rng(6)
+    N = 20000
+    counts = np.zeros(6)
+    for _ in range(N):
+        x = inverse_cdf(q, rng.random())
+        u = rng.random((1, 3)).astype(np.float32)
+        o = oracle_verify(zt, zd, np.array([[x]], np.int32), None, np.array([1.0], np.float32), u,
+                          top_k=np.array([k]), top_p=np.array([top_p]))
+        counts[o.out_tokens[0, 0]] += 1
+    assert counts[want == 0].sum() == 0
+    s = want > 0
+    assert stats.chisquare(counts[s], want[s] * N).pvalue > 1e-3
