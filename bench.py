@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--onehot", action="store_true",
                     help="one-hot drafts (greedy drafter): time spec_verify_onehot, no draft logits")
+    ap.add_argument("--filter", action="store_true",
+                    help="per-row top-k / top-p filtering of p and q before the test: time "
+                         "spec_verify_filtered on the workload with seeded top_k in {off, 20, 50, 100} "
+                         "and top_p in {off, 0.9, 0.95}")
     ap.add_argument("--rollback", action="store_true",
                     help="KV-cache rollback after a round: B=1024 rows of the default workload's draft "
                          "lengths, 320 KB cache entries (80 layers of K and V, 8 heads x 128, bf16)")
@@ -150,16 +154,17 @@ def workload_for(args, rank):
 # CPU baseline: the fp64 oracle, as it stands, on a bounded sample of the same workload
 # ------------------------------------------------------------------------------------------------
 
-def _oracle(w, onehot):
+def _oracle(w, onehot, filt=None):
     from oracle.spec_verify_oracle import oracle_verify, oracle_verify_onehot
     if onehot:
         return oracle_verify_onehot(w.target_logits, w.draft_tokens, w.draft_len, w.temperature,
                                     w.uniforms)
+    top_k, top_p = filt if filt is not None else (None, None)
     return oracle_verify(w.target_logits, w.draft_logits, w.draft_tokens, w.draft_len,
-                         w.temperature, w.uniforms)
+                         w.temperature, w.uniforms, top_k=top_k, top_p=top_p)
 
 
-def oracle_pool(cfg_key, seconds, seed=12345, onehot=False):
+def oracle_pool(cfg_key, seconds, seed=12345, onehot=False, filt=False):
     """Rows of the workload drawn on the host (numpy backend), as many as the oracle verifies in
     about `seconds` of single-thread CPU time (calibrated on 8 rows). Input generation is untimed."""
     import dataclasses
@@ -168,27 +173,34 @@ def oracle_pool(cfg_key, seconds, seed=12345, onehot=False):
 
     from workloads import get_config, make_workload
     cfg = get_config(cfg_key)
+    from workloads import filter_params
     probe = make_workload(dataclasses.replace(cfg, B=8), seed=seed, backend="numpy")
     t0 = time.perf_counter()
-    _oracle(probe, onehot)
+    _oracle(probe, onehot, filter_params(8, seed) if filt else None)
     t8 = time.perf_counter() - t0
     rows = int(max(8, min(cfg.B, round(seconds / max(t8, 1e-6) * 8 / 8) * 8)))
     w = make_workload(dataclasses.replace(cfg, B=rows), seed=seed + 1, backend="numpy")
+    if filt:
+        w.filters = filter_params(rows, seed + 1)
     return w, int(np.sum(w.draft_len.astype(np.int64) + 1))
 
 
 def oracle_run(w, onehot=False):
     """Wall seconds of one oracle pass over the pool's rows."""
     t0 = time.perf_counter()
-    _oracle(w, onehot)
+    _oracle(w, onehot, getattr(w, "filters", None))
     return time.perf_counter() - t0
 
 
-def oracle_sample_rate(cfg_key, seconds, onehot=False):
+def oracle_sample_rate(cfg_key, seconds, onehot=False, filt=False):
     """Oracle throughput (positions/s) on a bounded host-drawn sample of the workload."""
-    w, pos = oracle_pool(cfg_key, seconds, onehot=onehot)
+    w, pos = oracle_pool(cfg_key, seconds, onehot=onehot, filt=filt)
     secs = oracle_run(w, onehot)
     return pos / secs, w.B, pos, secs
+
+
+def workload_name(cfg, args):
+    return cfg.name + ("_onehot_drafts" if args.onehot else "") + ("_topk_topp" if args.filter else "")
 
 
 def run_reference_tree(args):
@@ -229,7 +241,7 @@ def run_reference(args):
     from workloads import get_config
     cfg = get_config(args.workload)
     per_step = 1.5      # seconds of single-thread oracle work per step
-    w, pos = oracle_pool(args.workload, per_step, onehot=args.onehot)
+    w, pos = oracle_pool(args.workload, per_step, onehot=args.onehot, filt=args.filter)
     for _ in range(args.warmup):
         oracle_run(w, args.onehot)
     total = 0.0
@@ -241,7 +253,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": cfg.name + ("_onehot_drafts" if args.onehot else ""), "B": cfg.B,
+        "config": {"workload": workload_name(cfg, args), "B": cfg.B,
                    "gamma_max": cfg.gamma_max, "V": cfg.V,
                    "logits": cfg.dtype, "sample_rows_per_step": w.B,
                    "sample_positions_per_step": pos},
@@ -281,9 +293,19 @@ def run_gpu(args):
 
     if args.onehot:                  # one-hot drafts: no draft logits exist
         del t["draft_logits"]
+    if args.filter:                  # per-row top-k / top-p, part of the step's inputs
+        from workloads import filter_params
+        fk, fp = filter_params(B, cfg.seed + 1000 * rank)
+        t["top_k"] = torch.from_numpy(fk).to(dev)
+        t["top_p"] = torch.from_numpy(fp).to(dev)
 
     def call(inp):
-        if args.onehot:
+        if args.filter:
+            sv.spec_verify_filtered(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
+                                    inp["draft_len"], inp["temperature"], inp["top_k"],
+                                    inp["top_p"], inp["uniforms"], out_tokens, out_num, out_alpha,
+                                    None, None, ws, stream)
+        elif args.onehot:
             sv.spec_verify_onehot(inp["target_logits"], inp["draft_tokens"], inp["draft_len"],
                                   inp["temperature"], inp["uniforms"], out_tokens, out_num,
                                   out_alpha, None, None, ws, stream)
@@ -332,7 +354,7 @@ def run_gpu(args):
     if TRAFFIC_FILE.exists():
         tr = json.loads(TRAFFIC_FILE.read_text())
         if tr.get("kernel_source_hash") == kernel_source_hash() and tr.get("workload") == cfg.name \
-                and not args.onehot:
+                and not args.onehot and not args.filter:
             traffic = tr["bytes_per_full_launch"]
 
     # ---- end to end: pinned host inputs -> device, the call, outputs -> pinned host ----
@@ -377,7 +399,8 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        rate, rows, pos, secs = oracle_sample_rate(args.workload, args.cpu_seconds, args.onehot)
+        rate, rows, pos, secs = oracle_sample_rate(args.workload, args.cpu_seconds, args.onehot,
+                                                   args.filter)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{rows} rows ({pos} positions) of the workload drawn on the host, "
                          f"{secs:.1f} s of single-thread fp64 oracle work"}
@@ -387,7 +410,7 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-            "config": {"workload": cfg.name + ("_onehot_drafts" if args.onehot else ""), "B": B,
+            "config": {"workload": workload_name(cfg, args), "B": B,
                        "gamma_max": G, "V": V, "logits": cfg.dtype,
                        "greedy_rows": int((w.temperature == 0).sum()),
                        "positions_per_gpu": positions, "padded_positions_per_gpu": B * (G + 1),
@@ -397,8 +420,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                          "frac": achieved_gbs / peak, "peak_kind": peak_kind,
                          "frac_of_8tbs": achieved_gbs / NORTH_STAR_HBM_GBS, "traffic": traffic,
-                         "kernel": "sv_stream_kernel<bf16>" if cfg.dtype == "bf16"
-                         else "sv_stream_kernel<f32>"},
+                         "kernel": ("sv_filter_kernel" if args.filter else "sv_stream_kernel")
+                         + ("<bf16>" if cfg.dtype == "bf16" else "<f32>")},
             "clocks": clock_info,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -171,6 +171,38 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
                             int32_t* out_pred, int32_t B, int32_t N, int32_t V, int32_t dtype,
                             void* workspace, size_t workspace_bytes, void* cuda_stream);
 
+/* Verification of filtered distributions: per-row top-k and top-p applied to p and q before the
+ * test. [R] "Speculative decoding", rayaq.ca ml-models -- Why the output is exactly the target's
+ * (temperature, top-p and any penalties are applied to p and q before the test; the rule then
+ * preserves exactly the distribution it is given). For a sampled row, p_i and q_i are replaced by
+ * filter(softmax(z / T)) with, in order:
+ *   top-k (0 < top_k[b] < V): keep the tokens whose logit is at least the top_k-th largest logit
+ *         (ties at the boundary all kept);
+ *   top-p (top_p[b] < 1): on the renormalised top-k distribution, keep a token when the mass of
+ *         the tokens with a strictly larger logit is below top_p[b] (tokens with equal logits go
+ *         together; the largest logit is always kept);
+ *   renormalise the kept probabilities.
+ * Then the rule of spec_verify on the filtered p~, q~: keep x_i while u[b,i] < min(1, p~(x)/q~(x))
+ * (q~(x) = 0 reads as 1); at the first rejection draw from max(0, p~ - q~) (from p~ when that has
+ * no mass) with u[b,G]; after gamma_b accepts draw the bonus from the filtered target p~ with
+ * u[b,G+1]; alpha_i = sum_v min(p~, q~); out_p_draft / out_q_draft are p~(x) and q~(x).
+ * Greedy rows are verified as in spec_verify (filtering keeps the argmax).
+ *
+ * top_k  [B] int32  per-row k; <= 0 or >= V turns top-k off. NULL: off for every row.
+ * top_p  [B] fp32   per-row nucleus mass; >= 1 turns top-p off; a sampled row with top_p NaN or
+ *                   <= 0 is a row error (outputs -1 / 0). NULL: off for every row.
+ * Everything else (arguments, layout, ownership, workspace, errors) as in spec_verify_ex. Only rows
+ * of 16-byte multiples are supported (else SV_ERR_BAD_SHAPE), with 16-byte aligned logit bases
+ * (else SV_ERR_MISALIGNED), and V at most 16 * 65536 bytes of logits per row (bf16 V <= 524288,
+ * fp32 V <= 262144; else SV_ERR_BAD_SHAPE). */
+int spec_verify_filtered(const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const int32_t* draft_len,
+                         const float* temperature, const int32_t* top_k, const float* top_p,
+                         const float* uniforms, int32_t* out_tokens, int32_t* out_num_emitted,
+                         float* out_alpha, float* out_p_draft, float* out_q_draft,
+                         int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                         void* workspace, size_t workspace_bytes, void* cuda_stream);
+
 /* KV-cache rollback after a verified round, batched over ragged rows. [R] "Speculative decoding",
  * rayaq.ca ml-models -- Verification attention and the cache: the target's cache held n entries
  * before the round and n + gamma + 1 after verification; with k drafts accepted the first n + k + 1

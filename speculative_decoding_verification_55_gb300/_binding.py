@@ -25,7 +25,8 @@ SV_ERR_SCRATCH_TOO_SMALL = 8
 SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_onehot",
-            "spec_verify_tree_greedy", "spec_verify_kv_rollback", "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
+            "spec_verify_filtered", "spec_verify_tree_greedy", "spec_verify_kv_rollback",
+            "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
             "spec_verify_version")
 
 _lib = None
@@ -60,6 +61,9 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_noalloc.restype = ctypes.c_int
             L.spec_verify_onehot.argtypes = [vp, i32p, i32p, f32p, f32p, i32p, i32p, f32p, f32p, f32p] + tail
             L.spec_verify_onehot.restype = ctypes.c_int
+            L.spec_verify_filtered.argtypes = [vp, vp, i32p, i32p, f32p, i32p, f32p, f32p, i32p, i32p,
+                                               f32p, f32p, f32p] + tail
+            L.spec_verify_filtered.restype = ctypes.c_int
             L.spec_verify_tree_greedy.argtypes = [vp, i32p, i32p, i32p, i32p, i32p, i32p, i32p] + tail
             L.spec_verify_tree_greedy.restype = ctypes.c_int
             L.spec_verify_kv_rollback.argtypes = [i32p, i32p, i32p, i32p, i32p, i32p, vp, ctypes.c_int64,
@@ -228,6 +232,41 @@ def spec_verify_onehot(target_logits, draft_tokens, draft_len, temperature, unif
         raise SpecVerifyError(st, "spec_verify_onehot")
 
 
+def spec_verify_filtered(target_logits, draft_logits, draft_tokens, draft_len, temperature, top_k,
+                         top_p, uniforms, out_tokens, out_num_emitted, out_alpha, out_p_draft,
+                         out_q_draft, workspace, stream=None) -> None:
+    """Calls the C ABI spec_verify_filtered (per-row top-k / top-p applied to p and q before the
+    test) on torch tensors; top_k [B] int32 and top_p [B] float32 may be None (off).
+    Raises SpecVerifyError on a nonzero status."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    _check(target_logits, "target_logits", device=dev)
+    _check(draft_logits, "draft_logits", dtype=target_logits.dtype, shape=(B, G, V), device=dev)
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, G), dev)
+    _check(draft_len, "draft_len", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(top_k, "top_k", torch.int32, (B,), dev)
+    _check(top_p, "top_p", torch.float32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, G + 2), dev)
+    _check(out_tokens, "out_tokens", torch.int32, (B, G + 1), dev)
+    _check(out_num_emitted, "out_num_emitted", torch.int32, (B,), dev)
+    for name, t in (("out_alpha", out_alpha), ("out_p_draft", out_p_draft),
+                    ("out_q_draft", out_q_draft)):
+        _check(t, name, torch.float32, (B, G), dev)
+    _check(workspace, "workspace", device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().spec_verify_filtered(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
+        _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(out_tokens),
+        _ptr(out_num_emitted), _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
+        B, G, V, _dtype_code(target_logits), _ptr(workspace), ws_bytes,
+        _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_filtered")
+
+
 def spec_verify_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size, out_path,
                             out_path_len, out_tokens, out_pred, workspace, stream=None) -> None:
     """Calls the C ABI spec_verify_tree_greedy (greedy verification of candidate trees) on torch
@@ -320,9 +359,10 @@ def workspace_for(B, G, V, dtype_code, device, stream=None):
 
 
 def verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
-           with_probs=False, stream=None, onehot=False):
+           with_probs=False, stream=None, onehot=False, top_k=None, top_p=None):
     """Allocates the outputs, runs spec_verify(_ex) (or spec_verify_onehot when ``onehot``: the
-    drafts are one-hot and draft_logits is ignored) and returns
+    drafts are one-hot and draft_logits is ignored; or spec_verify_filtered when ``top_k`` or
+    ``top_p`` is given) and returns
     (out_tokens [B, G+1], out_num_emitted [B], out_alpha [B, G][, out_p, out_q])."""
     import torch
     B, G1, V = target_logits.shape
@@ -334,7 +374,13 @@ def verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, un
     out_p = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
     out_q = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
     ws = workspace_for(B, G, V, _dtype_code(target_logits), dev, stream)
-    if onehot:
+    if top_k is not None or top_p is not None:
+        if onehot:
+            raise ValueError("filtering with one-hot drafts is not supported")
+        spec_verify_filtered(target_logits, draft_logits, draft_tokens, draft_len, temperature,
+                             top_k, top_p, uniforms, out_tokens, out_num, out_alpha, out_p, out_q,
+                             ws, stream)
+    elif onehot:
         spec_verify_onehot(target_logits, draft_tokens, draft_len, temperature, uniforms,
                            out_tokens, out_num, out_alpha, out_p, out_q, ws, stream)
     else:

@@ -67,6 +67,7 @@ int stream_cluster_size(long long row_bytes) {
 std::mutex g_mu;
 int g_device_ok[64];                 // 0 unknown, 1 sm_103, 2 other
 int g_max_clusters[64][2][5];        // by device, bf16, log2(C); 0 = not queried
+int g_filter_clusters[64][2][5];     // the same for the filter kernel
 
 int check_device(int* dev_out) {
   int dev = 0;
@@ -84,14 +85,16 @@ int check_device(int* dev_out) {
   return g_device_ok[dev] == 1 ? SV_OK : SV_ERR_UNSUPPORTED_DEVICE;
 }
 
-int max_clusters(int dev, bool bf16, int C, int* n) {
+int max_clusters(int dev, bool bf16, int C, int* n, bool filter = false) {
   int lg = 0;
   while ((1 << lg) < C) ++lg;
   std::lock_guard<std::mutex> lock(g_mu);
-  int& slot = g_max_clusters[dev][bf16 ? 1 : 0][lg];
+  int& slot = (filter ? g_filter_clusters : g_max_clusters)[dev][bf16 ? 1 : 0][lg];
   if (slot == 0) {
     int m = 0;
-    if (sv::stream_max_clusters(bf16, C, &m) != cudaSuccess || m < 1) return SV_ERR_CUDA;
+    const cudaError_t e =
+        filter ? sv::filter_max_clusters(bf16, C, &m) : sv::stream_max_clusters(bf16, C, &m);
+    if (e != cudaSuccess || m < 1) return SV_ERR_CUDA;
     slot = m;
   }
   *n = slot;
@@ -308,6 +311,75 @@ int spec_verify_onehot(const void* target_logits, const int32_t* draft_tokens,
   return verify_impl(target_logits, nullptr, draft_tokens, draft_len, temperature, uniforms,
                      out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft, B, gamma_max,
                      V, dtype, workspace, workspace_bytes, cuda_stream, true);
+}
+
+int spec_verify_filtered(const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const int32_t* draft_len,
+                         const float* temperature, const int32_t* top_k, const float* top_p,
+                         const float* uniforms, int32_t* out_tokens, int32_t* out_num_emitted,
+                         float* out_alpha, float* out_p_draft, float* out_q_draft,
+                         int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                         void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
+  if (!sizes_ok(B, gamma_max, V, dtype)) return SV_ERR_BAD_SHAPE;
+  const int G = gamma_max;
+  if (!target_logits || !temperature || !uniforms || !out_tokens || !out_num_emitted)
+    return SV_ERR_NULL_POINTER;
+  if (G > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_NULL_POINTER;
+  const bool bf16 = dtype == SV_DTYPE_BF16;
+  const uintptr_t es = bf16 ? 2 : 4;
+  auto mis = [](const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; };
+  if (mis(draft_tokens, 4) || mis(draft_len, 4) || mis(temperature, 4) || mis(top_k, 4) ||
+      mis(top_p, 4) || mis(uniforms, 4) || mis(out_tokens, 4) || mis(out_num_emitted, 4) ||
+      mis(out_alpha, 4) || mis(out_p_draft, 4) || mis(out_q_draft, 4) || mis(workspace, 16))
+    return SV_ERR_MISALIGNED;
+  // Rows of 16-byte multiples on 16-byte aligned bases only.
+  if ((static_cast<size_t>(V) * es) % 16 != 0) return SV_ERR_BAD_SHAPE;
+  if (mis(target_logits, 16) || mis(draft_logits, 16)) return SV_ERR_MISALIGNED;
+  const size_t need = spec_verify_workspace_size(B, G, V, dtype);
+  if (!workspace || workspace_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
+  if (static_cast<long long>(B) * (G + 1) > INT_MAX / sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
+  const int units = static_cast<int>(static_cast<size_t>(V) * es / 16);
+  int C = 1;
+  while ((units + C - 1) / C > sv::filter_max_row_units()) {
+    if (C >= sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
+    C *= 2;
+  }
+  int dev = 0;
+  const int dev_status = check_device(&dev);
+  if (dev_status != SV_OK) return dev_status;
+
+  sv::Params P{};
+  P.zt = target_logits;
+  P.zd = draft_logits;
+  P.tokens = draft_tokens;
+  P.draft_len = draft_len;
+  P.temperature = temperature;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.uniforms = uniforms;
+  P.out_tokens = out_tokens;
+  P.out_num = out_num_emitted;
+  P.out_alpha = out_alpha;
+  P.out_p = out_p_draft;
+  P.out_q = out_q_draft;
+  char* ws = static_cast<char*>(workspace);
+  P.rec = reinterpret_cast<int2*>(ws);
+  P.cnt = reinterpret_cast<unsigned*>(ws + records_bytes(B, G));
+  P.status = P.cnt + B;
+  P.B = B;
+  P.G = G;
+  P.V = V;
+  P.units = units;
+  P.C = C;
+  P.per = (units + C - 1) / C;
+  int maxc = 0;
+  if (max_clusters(dev, bf16, C, &maxc, true) != SV_OK) return SV_ERR_CUDA;
+  const long long slots = static_cast<long long>(B) * (G + 1);
+  P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
+  if (sv::launch_filter(P, bf16, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
 }
 
 int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,

@@ -58,6 +58,9 @@ struct Params {
   int32_t* out_path;         // [B, N] longest accepted path, root first
   int32_t* out_plen;         // [B] nodes on the path
   int32_t* out_pred;         // [B, N] target argmax per node, or null
+  // Filtered verification (filter kernel): per-row top-k and top-p, applied to p and q alike.
+  const int32_t* top_k;      // [B] or null (0 or >= V: off)
+  const float* top_p;        // [B] or null (>= 1: off)
 };
 
 constexpr int kMaxTreeNodes = 65;    // N <= SV_MAX_GAMMA + 1
@@ -627,5 +630,10 @@ cudaError_t launch_element(const Params& P, bool bf16, int vpt_index, cudaStream
 cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream);
 // Clusters of `C` CTAs of the streaming kernel that fit on the current device at once.
 cudaError_t stream_max_clusters(bool bf16, int C, int* n);
+// Filtered verification (16-byte aligned rows of at most 16 chunks of filter_max_row_units()
+// vectors): persistent clusters, one position per cluster at a time.
+cudaError_t launch_filter(Params P, bool bf16, cudaStream_t stream);
+cudaError_t filter_max_clusters(bool bf16, int C, int* n);
+int filter_max_row_units();
 
 }  // namespace sv

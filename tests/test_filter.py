@@ -188,3 +188,167 @@ def test_emitted_token_follows_the_filtered_target():
     assert counts[want == 0].sum() == 0
     s = want > 0
     assert stats.chisquare(counts[s], want[s] * N).pvalue > 1e-3
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU parity through the C ABI
+# ------------------------------------------------------------------------------------------------
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def sv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_55_gb300 as m
+    m.build_library()
+    return m
+
+
+def run_filtered(sv, zt, zd, x, n, T, u, top_k, top_p, dtype):
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
+    out = sv.verify(dev(zt).to(tdt), dev(zd).to(tdt), dev(x), dev(n), dev(T), dev(u),
+                    with_probs=True, top_k=None if top_k is None else dev(top_k),
+                    top_p=None if top_p is None else dev(top_p))
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in out]
+
+
+def check_filtered(zt, zd, x, n, T, u, top_k, top_p, gpu):
+    """Parity on every row whose filters are decided farther than the margin from top_p; the rest
+    are counted and must still be well formed."""
+    o = oracle_verify(zt, zd, x, n, T, u, diagnostics=True, top_k=top_k, top_p=top_p)
+    rows = [b for b in range(len(n)) if o.rows[b].filter_margin >= TOL]
+    rep = compare(o, *gpu, x, n, rows=rows)
+    assert rep.ok(), str(rep)
+    for b in set(range(len(n))) - set(rows):
+        assert 1 <= gpu[1][b] <= n[b] + 1
+    return rep, len(n) - len(rows)
+
+
+def filter_batch(B, G, V, dtype, seed, greedy_frac=0.15, ties=False):
+    """Seeded logits (drafts drawn from the filtered q~ with the oracle's own sampler), ragged
+    lengths, per-row top-k from {off, 1, 5, 50, V/2, V-1} and top-p from {off, 0.5, 0.9, 0.99, 1e-3}."""
+    rng = np.random.default_rng(seed)
+    zt = (rng.standard_normal((B, G + 1, V)) * 2.0).astype(np.float32)
+    zd = (zt[:, :G] + rng.standard_normal((B, G, V)).astype(np.float32) * 0.8).astype(np.float32)
+    if ties:
+        zt, zd = np.round(zt * 2) / 2, np.round(zd * 2) / 2
+    if dtype == "bf16":
+        zt, zd = bf16_round(zt), bf16_round(zd)
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    T[rng.random(B) < greedy_frac] = 0.0
+    n = rng.integers(0, G + 1, B).astype(np.int32)
+    n[0] = G
+    top_k = rng.choice(np.array([0, 1, 5, 50, V // 2, V - 1], np.int64), B).astype(np.int32)
+    top_p = rng.choice(np.array([1.0, 0.5, 0.9, 0.99, 1e-3], np.float32), B).astype(np.float32)
+    u = rng.random((B, G + 2), dtype=np.float32)
+    x = np.full((B, G), -1, np.int32)
+    for b in range(B):
+        for i in range(n[b]):
+            if T[b] == 0:
+                x[b, i] = int(np.argmax(zd[b, i]))
+            else:
+                q, _ = filtered_softmax(zd[b, i], T[b], int(top_k[b]), np.float64(top_p[b]))
+                x[b, i] = inverse_cdf(q, rng.random())
+        zt[b, n[b] + 1:] = np.nan
+        zd[b, n[b]:] = np.nan
+    return zt, zd, x, n, T, u, top_k, top_p
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,V,B,G", [("f32", 256, 16, 4), ("bf16", 1000, 16, 4),
+                                         ("f32", 4100, 12, 5), ("bf16", 32000, 12, 4),
+                                         ("bf16", 128256, 6, 3), ("f32", 152064, 4, 3)])
+def test_gpu_filtered_random_batches(sv, dtype, V, B, G):
+    args = filter_batch(B, G, V, dtype, seed=V + B)
+    gpu = run_filtered(sv, *args, dtype)
+    rep, skipped = check_filtered(*args, gpu)
+    print(f"{dtype} V={V}: {rep} filter-margin rows={skipped}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gpu_filtered_ties_and_degenerate_rows(sv, dtype):
+    """Heavy ties at the top-k boundary and inside the nucleus, rows of equal logits, rows with
+    -inf logits (fewer finite logits than k), and top-p / top-k at their extremes."""
+    B, G, V = 12, 3, 5000
+    zt, zd, x, n, T, u, top_k, top_p = filter_batch(B, G, V, dtype, seed=7, greedy_frac=0.0,
+                                                    ties=True)
+    zt[1, :2] = 0.75                       # equal logits: every filter keeps every token
+    zd[1, :2] = 0.75
+    top_k[1], top_p[1] = 3, np.float32(0.5)
+    zt[2, 0, 100:] = -np.inf               # only 100 finite logits at position 0, k beyond them
+    zd[2, 0, 100:] = -np.inf
+    top_k[2], top_p[2] = 300, np.float32(1.0)
+    top_k[3], top_p[3] = 1, np.float32(1.0)
+    top_k[4], top_p[4] = V - 1, np.float32(0.999999)
+    top_k[5], top_p[5] = 0, np.float32(1e-7)
+    for b in (1, 2, 3, 4, 5):
+        n[b] = G
+        zt_b = zt[b, :n[b] + 1]
+        zt_b[np.isnan(zt_b)] = 0.0
+        zd_b = zd[b, :n[b]]
+        zd_b[np.isnan(zd_b)] = 0.0
+        for i in range(n[b]):
+            q, _ = filtered_softmax(zd[b, i], T[b], int(top_k[b]), np.float64(top_p[b]))
+            x[b, i] = inverse_cdf(q, 0.37)
+    gpu = run_filtered(sv, zt, zd, x, n, T, u, top_k, top_p, dtype)
+    check_filtered(zt, zd, x, n, T, u, top_k, top_p, gpu)
+
+
+@pytest.mark.gpu
+def test_gpu_filtered_row_errors(sv):
+    B, G, V = 6, 2, 2048
+    zt, zd, x, n, T, u, top_k, top_p = filter_batch(B, G, V, "f32", seed=8, greedy_frac=0.0)
+    n[:] = G
+    for b in range(B):
+        for i in range(G):
+            x[b, i] = int(np.argmax(zd[b, i]))
+    zt[:, :] = np.where(np.isnan(zt), 0.0, zt)
+    zd[:, :] = np.where(np.isnan(zd), 0.0, zd)
+    top_p[0], top_p[1], top_p[2] = 0.0, -1.0, np.nan
+    T[3], top_p[3] = 0.0, 0.0             # greedy row: top-p does not apply
+    gpu = run_filtered(sv, zt, zd, x, n, T, u, top_k, top_p, "f32")
+    assert (gpu[1][:3] == -1).all() and gpu[1][3] >= 1
+    check_filtered(zt, zd, x, n, T, u, top_k, top_p, gpu)
+
+
+@pytest.mark.gpu
+def test_gpu_filters_off_match_the_plain_kernel(sv):
+    """Filters off (the filter kernel) and top_k / top_p None (the streaming kernel) both match
+    the plain oracle."""
+    B, G, V = 16, 4, 32000
+    zt, zd, x, n, T, u, _, _ = filter_batch(B, G, V, "bf16", seed=9)
+    a = run_filtered(sv, zt, zd, x, n, T, u, np.zeros(B, np.int32), np.ones(B, np.float32), "bf16")
+    b = run_filtered(sv, zt, zd, x, n, T, u, None, None, "bf16")
+    o = oracle_verify(zt, zd, x, n, T, u, diagnostics=True)
+    for g in (a, b):
+        rep = compare(o, *g, x, n)
+        assert rep.ok(), str(rep)
+
+
+@pytest.mark.gpu
+def test_gpu_filtered_full_size_sampled_rows(sv):
+    """The benchmark's filtered step (B=1024, ragged, V=256000 bf16, seeded top-k / top-p per row)
+    in one launch; the oracle checks a sample of rows."""
+    from workloads import filter_params, make_workload
+    w = make_workload(5, backend="torch", device="cuda")
+    top_k, top_p = filter_params(w.B, w.cfg.seed)
+    t = w.device_tensors()
+    out = sv.verify(t["target_logits"], t["draft_logits"], t["draft_tokens"], t["draft_len"],
+                    t["temperature"], t["uniforms"], with_probs=True,
+                    top_k=torch.from_numpy(top_k).cuda(), top_p=torch.from_numpy(top_p).cuda())
+    torch.cuda.synchronize()
+    gpu = [o.cpu().numpy() for o in out]
+    rows = sorted({0, w.B - 1, *np.flatnonzero(w.temperature == 0)[:2].tolist(),
+                   *np.random.default_rng(10).integers(w.B, size=14).tolist()})
+    idx = np.asarray(rows)
+    zt = np.stack([w.host_rows(b)[0] for b in rows])
+    zd = np.stack([w.host_rows(b)[1] for b in rows])
+    check_filtered(zt, zd, w.draft_tokens[idx], w.draft_len[idx], w.temperature[idx],
+                   w.uniforms[idx], top_k[idx], top_p[idx], [a[idx] for a in gpu])
+    num = gpu[1]
+    assert ((num >= 1) & (num <= w.draft_len + 1)).all()

@@ -4,4 +4,5 @@ This package is shared by the GPU tests, the benchmark and the oracle's tests. I
 numbers and lays them out; it holds none of the verification arithmetic.
 """
 from .configs import CONFIGS, Config, get_config  # noqa: F401
-from .generate import Workload, make_workload, bf16_round, bf16_bits_to_f32  # noqa: F401
+from .generate import (Workload, bf16_bits_to_f32, bf16_round, filter_params,  # noqa: F401
+                       make_workload)

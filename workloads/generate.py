@@ -140,6 +140,15 @@ class Workload:
         )
 
 
+def filter_params(B, seed):
+    """Per-row sampling filters of a serving batch: top_k [B] int32 drawn from {0 (off), 20, 50, 100}
+    and top_p [B] float32 from {1.0 (off), 0.9, 0.95}, seeded."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 7]))
+    top_k = rng.choice(np.array([0, 20, 50, 100], dtype=np.int32), size=B).astype(np.int32)
+    top_p = rng.choice(np.array([1.0, 0.9, 0.95], dtype=np.float32), size=B).astype(np.float32)
+    return top_k, top_p
+
+
 def _gumbel_argmax_np(zd_rows, T, rng):
     g = rng.random(zd_rows.shape)
     g = -np.log(-np.log(np.clip(g, 1e-300, None)))
