@@ -162,134 +162,6 @@ __device__ __forceinline__ void set_status(const Params& P, Shared& sm, unsigned
   sm.stop = 1;
 }
 
-// Pass-1 update of a running (max m, sum s) with the 8 or 4 logits of one vector.
-template <bool BF16>
-__device__ __forceinline__ void online_update(const uint4& v, float k, float& m, f32x2& s, float& mx) {
-  const float vm = vec_max<BF16>(v);
-  mx = max_nan(mx, vm);
-  if (vm > m) {                                   // rescale the running sum to the new max
-    float s0, s1;
-    upk(s, s0, s1);
-    const float f = ex2((m - vm) * k);
-    s = pk(s0 * f, s1 * f);
-    m = vm;
-  }
-  const float c = -m * k;
-  const f32x2 k2 = pk(k, k), c2 = pk(c, c);
-  if (BF16) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float a0, a1;
-      upk(fma2(pk(bf_lo(w[j]), bf_hi(w[j])), k2, c2), a0, a1);
-      s = add2(s, pk(ex2(a0), ex2(a1)));
-    }
-  } else {
-    float a0, a1, a2, a3;
-    upk(fma2(pk(__uint_as_float(v.x), __uint_as_float(v.y)), k2, c2), a0, a1);
-    upk(fma2(pk(__uint_as_float(v.z), __uint_as_float(v.w)), k2, c2), a2, a3);
-    s = add2(s, pk(ex2(a0), ex2(a1)));
-    s = add2(s, pk(ex2(a2), ex2(a3)));
-  }
-}
-
-// Pass-1 update with the kUnitsPerSlot vectors one thread takes from a ring slot: one max and one
-// rescale check for the batch, then every exp2 with two independent accumulators.
-template <bool BF16, int N>
-__device__ __forceinline__ void online_update_batch(const uint4 (&v)[N], float k, float& m, f32x2& s,
-                                                    float& mx) {
-  float vm = -INFINITY;
-  if (BF16) {
-    uint32_t a = bmax2_nan(bmax2_nan(v[0].x, v[0].y), bmax2_nan(v[0].z, v[0].w));
-#pragma unroll
-    for (int j = 1; j < N; ++j)
-      a = bmax2_nan(a, bmax2_nan(bmax2_nan(v[j].x, v[j].y), bmax2_nan(v[j].z, v[j].w)));
-    vm = max_nan(bf_lo(a), bf_hi(a));
-  } else {
-#pragma unroll
-    for (int j = 0; j < N; ++j) vm = max_nan(vm, vec_max<false>(v[j]));
-  }
-  mx = max_nan(mx, vm);
-  if (vm > m) {                                   // rescale the running sum to the new max
-    float s0, s1;
-    upk(s, s0, s1);
-    const float f = ex2((m - vm) * k);
-    s = pk(s0 * f, s1 * f);
-    m = vm;
-  }
-  const float c = -m * k;
-  const f32x2 k2 = pk(k, k), c2 = pk(c, c);
-  f32x2 acc[4] = {pk(0.0f, 0.0f), pk(0.0f, 0.0f), pk(0.0f, 0.0f), pk(0.0f, 0.0f)};
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float a0, a1;
-      if (BF16) {
-        upk(fma2(pk(bf_lo(w[q]), bf_hi(w[q])), k2, c2), a0, a1);
-      } else {
-        if (q >= 2) break;
-        upk(fma2(pk(__uint_as_float(w[2 * q]), __uint_as_float(w[2 * q + 1])), k2, c2), a0, a1);
-      }
-      acc[(j * 4 + q) & 3] = add2(acc[(j * 4 + q) & 3], pk(ex2(a0), ex2(a1)));
-    }
-  }
-  s = add2(s, add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])));
-}
-
-// Pass-1 greedy update: running max and the lowest index holding it.
-template <bool BF16>
-__device__ __forceinline__ void argmax_update(const uint4& v, int base, float& m, int& idx, float& mx) {
-  constexpr int E = BF16 ? 8 : 4;
-  const float vm = vec_max<BF16>(v);
-  mx = max_nan(mx, vm);
-  if (vm > m) {
-#pragma unroll
-    for (int e = E - 1; e >= 0; --e)
-      if (vec_get<BF16>(v, e) == vm) idx = base + e;
-    m = vm;
-  }
-}
-
-// Residual weights max(0, p - q) of element pair e, e+1 of a target vector and its draft vector,
-// p and q normalised inside the exponent (ct, cd), two logits per packed instruction.
-template <bool BF16>
-__device__ __forceinline__ void resid_pair(const uint4& t, const uint4& d, int e, f32x2 k2, f32x2 c2,
-                                           float& w0, float& w1) {
-  float a0, b0, a1, b1;
-  upk(fma2(pk(vec_get<BF16>(t, e), vec_get<BF16>(d, e)), k2, c2), a0, b0);
-  upk(fma2(pk(vec_get<BF16>(t, e + 1), vec_get<BF16>(d, e + 1)), k2, c2), a1, b1);
-  upk(sub2(pk(ex2(a0), ex2(a1)), pk(ex2(b0), ex2(b1))), w0, w1);
-  w0 = fmaxf(w0, 0.0f);
-  w1 = fmaxf(w1, 0.0f);
-}
-
-// Sum of the residual weights of one vector pair (the order the draw's rescan reproduces).
-template <bool BF16>
-__device__ __forceinline__ float resid_vec_sum(const uint4& t, const uint4& d, f32x2 k2, f32x2 c2) {
-  constexpr int E = BF16 ? 8 : 4;
-  float w[E];
-#pragma unroll
-  for (int e = 0; e < E; e += 2) resid_pair<BF16>(t, d, e, k2, c2, w[e], w[e + 1]);
-#pragma unroll
-  for (int h = 1; h < E; h *= 2) {
-#pragma unroll
-    for (int e = 0; e < E; e += 2 * h) w[e] += w[e + h];
-  }
-  return w[0];
-}
-
-// Sum of the unnormalised p weights exp2(z k + cb) of one vector.
-template <bool BF16>
-__device__ __forceinline__ float p_vec_sum(const uint4& t, float k, float cb) {
-  constexpr int E = BF16 ? 8 : 4;
-  float s = 0.0f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) s += ex2(fmaf(vec_get<BF16>(t, e), k, cb));
-  return s;
-}
-
 // The vector with element e set to -inf (a one-hot draft's token, left out of a sum).
 template <bool BF16>
 __device__ __forceinline__ uint4 mask_elem(uint4 v, int e) {

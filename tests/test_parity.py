@@ -184,6 +184,25 @@ def test_all_greedy_and_argmax_ties(sv):
     check(oracle_verify(*args, diagnostics=True), gpu, tokens, draft_len)
 
 
+@pytest.mark.parametrize("dtype,V,runs", [("bf16", 32768, [(0, 8192)]),
+                                           ("f32", 32768, [(0, 4096), (16384, 20480)])])
+def test_leading_neg_inf_runs(sv, dtype, V, runs):
+    """Runs of -inf logits at the start of the row's chunks: every thread's first batch of logits
+    is -inf and its finite logits come later (a running max of -inf must not poison the sum)."""
+    B, G = 6, 3
+    zt, zd, _, draft_len, temperature, u = small_inputs(B, G, V, dtype, seed=31, greedy_frac=0.2,
+                                                        ragged=False)
+    for a, b in runs:
+        zt[:, :, a:b] = -np.inf
+        zd[:, :, a:b] = -np.inf
+    rng = np.random.default_rng(32)
+    tokens = sample_drafts(zd, temperature, rng.random((B, G), dtype=np.float32))
+    args = (zt, zd, tokens, draft_len, temperature, u)
+    gpu = run_gpu(sv, to_dev(*args, dtype))
+    check(oracle_verify(*args, diagnostics=True), gpu, tokens, draft_len)
+    assert (gpu[1] >= 1).all()
+
+
 def test_zero_draft_mass_and_equal_rows(sv):
     B, G, V = 6, 3, 512
     rng = np.random.default_rng(9)
