@@ -37,8 +37,11 @@ constexpr int kFT = 512;                        // threads per CTA
 constexpr int kFW = kFT / 32;
 constexpr int kFRowBytes = 65536;               // a row chunk held in shared memory
 constexpr int kFRowUnits = kFRowBytes / 16;
-constexpr int kFDynBytes = 2 * kFRowBytes;
 constexpr int kBins = 256;
+// Per-warp histograms (count and mass per row and bin) beside the two row chunks: a warp's atomics
+// only meet its own lanes'.
+constexpr int kHistBytes = kFW * 2 * kBins * 8;
+constexpr int kFDynBytes = 2 * kFRowBytes + kHistBytes;
 constexpr int kCopyPiece = 16384;               // bytes per bulk copy
 constexpr float kBinsPerLog2 = 8.0f;            // level-0 resolution
 
@@ -507,21 +510,23 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
         }
         __syncthreads();
         while (sm.sel[0].act || (nrows > 1 && sm.sel[1].act)) {
-          // histograms of the active rows' candidates
+          // histograms of the active rows' candidates: per warp, then summed over the warps in order
           const uint32_t par = ex & 1;
-          for (int j = tid; j < 2 * kBins; j += kFT) {
-            (&sm.hc[par][0][0])[j] = 0u;
-            (&sm.hm[par][0][0])[j] = 0.0f;
+          unsigned* whc = reinterpret_cast<unsigned*>(dyn + 2 * kFRowBytes) + warp * 2 * kBins;
+          float* whm = reinterpret_cast<float*>(dyn + 2 * kFRowBytes + kFW * 2 * kBins * 4) + warp * 2 * kBins;
+          for (int j = lane; j < 2 * kBins; j += 32) {
+            whc[j] = 0u;
+            whm[j] = 0.0f;
           }
-          __syncthreads();
+          __syncwarp();
           for (int r = 0; r < nrows; ++r) {
             const FSel S = sm.sel[r];
             if (!S.act) continue;
             const uint4* src = r == 0 ? dt : dd;
             const float Mr = M[r];
             const int sh = KB - 8 * S.lvl;
-            unsigned* hc = sm.hc[par][r];
-            float* hm = sm.hm[par][r];
+            unsigned* hc = whc + r * kBins;
+            float* hm = whm + r * kBins;
             for (int u = tid; u < cu; u += kFT) {
               const uint4 v = src[u];
 #pragma unroll
@@ -542,6 +547,24 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
               }
             }
           }
+          __syncthreads();
+          {
+            const unsigned* ahc = reinterpret_cast<const unsigned*>(dyn + 2 * kFRowBytes);
+            const float* ahm = reinterpret_cast<const float*>(dyn + 2 * kFRowBytes + kFW * 2 * kBins * 4);
+            for (int j = tid; j < 2 * kBins; j += kFT) {
+              unsigned c = 0u;
+              float mm = 0.0f;
+              if (j / kBins < nrows) {
+#pragma unroll 4
+                for (int w = 0; w < kFW; ++w) {
+                  c += ahc[w * 2 * kBins + j];
+                  mm += ahm[w * 2 * kBins + j];
+                }
+              }
+              (&sm.hc[par][0][0])[j] = c;
+              (&sm.hm[par][0][0])[j] = mm;
+            }
+          }
           publish();
           // the cluster's histograms, summed in rank order
           for (int j = tid; j < 2 * kBins; j += kFT) {
@@ -549,11 +572,25 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
             unsigned c = 0u;
             float mm = 0.0f;
             if (r < nrows && sm.sel[r].act) {
+              // Every peer's entry is requested before any is added, so the remote latencies overlap;
+              // the sums then run in rank order.
               const uint32_t ac = smem_addr(&sm.hc[par][0][0] + j);
               const uint32_t am = smem_addr(&sm.hm[par][0][0] + j);
-              for (int q = 0; q < C; ++q) {
-                c += static_cast<unsigned>(ld_cluster_s32(map_to_rank(ac, static_cast<uint32_t>(q))));
-                mm += ld_cluster_f32(map_to_rank(am, static_cast<uint32_t>(q)));
+              int cq[kMaxCluster];
+              float mq[kMaxCluster];
+#pragma unroll
+              for (int q = 0; q < kMaxCluster; ++q) {
+                if (q < C) {
+                  cq[q] = ld_cluster_s32(map_to_rank(ac, static_cast<uint32_t>(q)));
+                  mq[q] = ld_cluster_f32(map_to_rank(am, static_cast<uint32_t>(q)));
+                }
+              }
+#pragma unroll
+              for (int q = 0; q < kMaxCluster; ++q) {
+                if (q < C) {
+                  c += static_cast<unsigned>(cq[q]);
+                  mm += mq[q];
+                }
               }
             }
             (&sm.gc[0][0])[j] = c;
