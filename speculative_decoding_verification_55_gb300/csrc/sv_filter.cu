@@ -527,22 +527,28 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
             const int sh = KB - 8 * S.lvl;
             unsigned* hc = whc + r * kBins;
             float* hm = whm + r * kBins;
+            // The value bin rules out almost every logit at the deeper levels (and, under a lower
+            // bound, at level 0); the order key is computed only for the logits it leaves.
+            const int binlo = S.lvl == 0 ? S.lbD0 : S.D0;
+            const int binhi = S.lvl == 0 ? 255 : S.D0;
             for (int u = tid; u < cu; u += kFT) {
               const uint4 v = src[u];
 #pragma unroll
               for (int e = 0; e < E; ++e) {
                 const float z = vec_get<BF16>(v, e);
                 const int vb = vbin(z, Mr, k);
-                const uint32_t key = okey<BF16>(z);
-                bool cand = at_or_above(vb, key, S.lbD0, S.lbkey);
-                int digit = vb;
-                if (S.lvl > 0) {
-                  cand = cand && vb == S.D0 && (S.lvl == 1 || (key >> (sh + 8)) == S.pre);
-                  digit = static_cast<int>((key >> sh) & 255u);
-                }
-                if (cand) {
-                  atomicAdd(hc + digit, 1u);
-                  atomicAdd(hm + digit, ex2((z - Mr) * k));
+                if (vb >= binlo && vb <= binhi) {
+                  const uint32_t key = okey<BF16>(z);
+                  bool cand = vb != S.lbD0 || key >= S.lbkey;
+                  int digit = vb;
+                  if (S.lvl > 0) {
+                    cand = cand && (S.lvl == 1 || (key >> (sh + 8)) == S.pre);
+                    digit = static_cast<int>((key >> sh) & 255u);
+                  }
+                  if (cand) {
+                    atomicAdd(hc + digit, 1u);
+                    atomicAdd(hm + digit, ex2((z - Mr) * k));
+                  }
                 }
               }
             }
@@ -618,7 +624,9 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
 
     // ---- V: the filtered p~ (and q~), the accept test, the chunk totals ----
     auto kept = [&](float z, int r) -> bool {
-      return !filt || at_or_above(vbin(z, M[r], k), okey<BF16>(z), thD0[r], thkey[r]);
+      if (!filt) return true;
+      const int vb = vbin(z, M[r], k);
+      return vb > thD0[r] || (vb == thD0[r] && okey<BF16>(z) >= thkey[r]);
     };
     const float lt = -log2f(Sk[0]);              // p~(v) = exp2((z - M) k - log2 Sk) on kept logits
     const float ld = p.two ? -log2f(Sk[1]) : 0.0f;
