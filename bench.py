@@ -71,6 +71,27 @@ def dist_env():
     return world, rank, local
 
 
+def rank_seed(base_seed, rank):
+    """The workload seed of one rank: every rank verifies its own independent batch (weak scaling,
+    the rows shard across GPUs with no exchange)."""
+    return base_seed + 1000 * rank
+
+
+def job_totals(ms, units, device=None):
+    """Whole-job figures of a run over every rank of the process group: the slowest rank's
+    milliseconds (each timed region ends at a barrier that waits for it) and the units all ranks
+    processed (ragged batches give each rank its own count). One rank: the inputs themselves."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms), float(units)
+    slowest = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    done = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(slowest, op=dist.ReduceOp.MAX)
+    dist.all_reduce(done, op=dist.ReduceOp.SUM)
+    return float(slowest.item()), float(done.item())
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
@@ -144,7 +165,7 @@ def workload_for(args, rank):
     from workloads import get_config, make_workload
     import dataclasses
     cfg = get_config(args.workload)
-    seed = cfg.seed + 1000 * rank
+    seed = rank_seed(cfg.seed, rank)
     if args.rows:
         cfg = dataclasses.replace(cfg, B=min(args.rows, cfg.B))
     return cfg, make_workload(cfg, seed=seed, backend="torch", device="cuda")
@@ -295,7 +316,7 @@ def run_gpu(args):
         del t["draft_logits"]
     if args.filter:                  # per-row top-k / top-p, part of the step's inputs
         from workloads import filter_params
-        fk, fp = filter_params(B, cfg.seed + 1000 * rank)
+        fk, fp = filter_params(B, rank_seed(cfg.seed, rank))
         t["top_k"] = torch.from_numpy(fk).to(dev)
         t["top_p"] = torch.from_numpy(fp).to(dev)
 
@@ -339,13 +360,9 @@ def run_gpu(args):
     barrier()
     ms_total = ev0.elapsed_time(ev1)
     clock_info = clocks.stop()
-    ms_step = ms_total / args.steps
-    if world > 1:
-        mt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(mt.item())
     positions = w.positions()
-    value = positions * world / (ms_step * 1e-3)
+    ms_step, positions_all = job_totals(ms_total / args.steps, positions, dev)
+    value = positions_all / (ms_step * 1e-3)
     algo_bytes = w.algorithmic_bytes(onehot=args.onehot)
     achieved_gbs = algo_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
@@ -387,12 +404,8 @@ def run_gpu(args):
             e2e_step()
         e1.record(stream)
         barrier()
-        ms_e2e = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            mt = torch.tensor([ms_e2e], device=dev)
-            torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
-            ms_e2e = float(mt.item())
-        e2e = {"value": positions * world / (ms_e2e * 1e-3), "unit": UNIT,
+        ms_e2e, _ = job_totals(e0.elapsed_time(e1) / n_e2e, positions, dev)
+        e2e = {"value": positions_all / (ms_e2e * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "ms_per_step": ms_e2e, "steps": n_e2e}
         del host, dev_in
@@ -413,7 +426,8 @@ def run_gpu(args):
             "config": {"workload": workload_name(cfg, args), "B": B,
                        "gamma_max": G, "V": V, "logits": cfg.dtype,
                        "greedy_rows": int((w.temperature == 0).sum()),
-                       "positions_per_gpu": positions, "padded_positions_per_gpu": B * (G + 1),
+                       "positions_per_gpu": positions, "positions_all_gpus": int(positions_all),
+                       "padded_positions_per_gpu": B * (G + 1),
                        "algorithmic_bytes_per_step": algo_bytes,
                        "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
             "gpu_launches": args.steps,
@@ -494,7 +508,7 @@ def run_tree(args):
     import speculative_decoding_verification_55_gb300 as sv
     sv.build_library()
     B = min(args.rows, TREE_B) if args.rows else TREE_B
-    zt, tok, par = tree_inputs(B, 7 + 1000 * rank, "torch")
+    zt, tok, par = tree_inputs(B, rank_seed(7, rank), "torch")
     N = zt.shape[1]
     stream = torch.cuda.current_stream(dev)
     ws = sv.workspace_for(B, N - 1, TREE_V, sv.SV_DTYPE_BF16, dev, stream)
@@ -523,13 +537,9 @@ def run_tree(args):
         call(zt, tok, par)
     ev1.record(stream)
     barrier()
-    ms_step = ev0.elapsed_time(ev1) / args.steps
     clock_info = clocks.stop()
-    if world > 1:
-        mt = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(mt, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(mt.item())
     nodes = B * N
+    ms_step, nodes_all = job_totals(ev0.elapsed_time(ev1) / args.steps, nodes, dev)
     algo = B * N * TREE_V * 2 + B * N * 8 + B * (N + N + 1 + N + 1) * 4
     achieved = algo / (ms_step * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
@@ -559,8 +569,8 @@ def run_tree(args):
             e2e_step()
         e1.record(stream)
         barrier()
-        ms_e2e = e0.elapsed_time(e1) / n_e2e
-        e2e = {"value": nodes * world / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
+        ms_e2e, _ = job_totals(e0.elapsed_time(e1) / n_e2e, nodes, dev)
+        e2e = {"value": nodes_all / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(bi),
                "d2h_bytes_per_step": int(bo), "ms_per_step": ms_e2e, "steps": n_e2e}
 
     cpu = None
@@ -575,7 +585,7 @@ def run_tree(args):
                          f"fp64 oracle work"}
     if rank == 0:
         line = {
-            "metric": METRIC, "value": nodes * world / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": nodes_all / (ms_step * 1e-3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
