@@ -32,7 +32,7 @@ sys.path.insert(0, str(ROOT))
 
 METRIC = "verified positions/sec (B·(γ+1)) and logits HBM GB/s vs 8 TB/s roofline"
 UNIT = "positions/s"
-NORTH_STAR_HBM_GBS = 8000.0
+NOMINAL_HBM_GBS = 8000.0
 DEFAULT_WORKLOAD = 5
 TRAFFIC_FILE = ROOT / "profiles" / "sv_stream_kernel_traffic.json"
 KERNEL_SOURCES = ["sv_stream.cu", "sv_common.cuh", "sv_api.cu"]
@@ -433,7 +433,7 @@ def run_gpu(args):
             "gpu_launches": args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                          "frac": achieved_gbs / peak, "peak_kind": peak_kind,
-                         "frac_of_8tbs": achieved_gbs / NORTH_STAR_HBM_GBS, "traffic": traffic,
+                         "frac_of_8tbs": achieved_gbs / NOMINAL_HBM_GBS, "traffic": traffic,
                          "kernel": ("sv_filter_kernel" if args.filter else "sv_stream_kernel")
                          + ("<bf16>" if cfg.dtype == "bf16" else "<f32>")},
             "clocks": clock_info,
@@ -596,7 +596,7 @@ def run_tree(args):
             "gpu_launches": args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
-                         "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "traffic": None,
+                         "frac_of_8tbs": achieved / NOMINAL_HBM_GBS, "traffic": None,
                          "kernel": "sv_stream_kernel<bf16>"},
             "clocks": clock_info, "e2e": e2e, "cpu_baseline": cpu,
         }
@@ -688,7 +688,7 @@ def run_rollback(args):
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "frac_of_8tbs": achieved / NORTH_STAR_HBM_GBS, "traffic": None,
+                     "frac_of_8tbs": achieved / NOMINAL_HBM_GBS, "traffic": None,
                      "kernel": "sv_rollback_kernel"},
         "clocks": clock_info, "e2e": None, "cpu_baseline": None,
     }

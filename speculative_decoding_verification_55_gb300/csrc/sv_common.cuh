@@ -141,14 +141,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   return pol;
 }
 
-__device__ __forceinline__ uint4 ld_stream_v4_hint(const void* p, uint64_t pol) {
-  uint4 r;
-  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-      : "l"(p), "l"(pol));
-  return r;
-}
-
 // One stored logit widened to fp32 (exact for both storage types).
 template <bool BF16>
 __device__ __forceinline__ float load_logit(const void* row, int v) {
@@ -220,15 +212,6 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_v4f32(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
-               ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
-
 // Asynchronous stores into another CTA's shared memory that complete their bytes on that CTA's
 // mbarrier (no fence, no round trip for the storing thread).
 __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -271,32 +254,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Non-blocking test of a phase (for a thread that serves several barriers in turn).
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// One poll that may suspend the thread for up to `ns` nanoseconds while the phase is incomplete.
-__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }

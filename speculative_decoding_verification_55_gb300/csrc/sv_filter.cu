@@ -24,6 +24,11 @@
 //       holding the draw's threshold (the residual draw, its fallback to p~, or the bonus draw).
 //   D   that CTA scans its chunk in index order (block-wide prefix sum over per-thread runs) and
 //       finishes the position; the row's last finished position emits the row (finish_position).
+//   L   a position with top-k takes a shorter road first: one count pass over the value bins near
+//       the max gives the bin of the k-th largest logit, one pass writes every logit of that bin
+//       or above (a superset of the top-k set, typically k plus a few) into a per-CTA list, and
+//       when the lists fit, rank 0 gathers them in index order and runs K, P, V and D on them
+//       alone while the other CTAs move on. Same levels and decisions as the chunk-wide passes.
 // Control flow depends on cluster-wide data only, so every CTA passes the same cluster barriers.
 // The bulk-copy wait is bounded; a CTA whose wait gives up reports it in the next exchange, the
 // position is marked bad, the status word is set and the cluster stops.
@@ -44,6 +49,13 @@ constexpr int kHistBytes = kFW * 2 * kBins * 8;
 constexpr int kFDynBytes = 2 * kFRowBytes + kHistBytes;
 constexpr int kCopyPiece = 16384;               // bytes per bulk copy
 constexpr float kBinsPerLog2 = 8.0f;            // level-0 resolution
+// Top-k rows: the count pass counts the value bins from kLowBin up (logits within 24 units of log2
+// probability of the max); a candidate list holds at most kLCap logits of a row, per CTA and for
+// the whole cluster. The target list's four arrays and the draft list's one sit where the per-warp
+// histograms were, the rank-0 gathered lists after them.
+constexpr int kLowBin = 64;
+constexpr int kLCap = 1024;
+static_assert(9 * kLCap * 4 <= kHistBytes, "candidate lists exceed the histogram area");
 
 enum : unsigned { kStatusTimeout = 1u };
 
@@ -76,6 +88,15 @@ struct FShared {
   float bc[16];                                 // broadcast of cluster-wide values
   int bi[16];
   int stop;
+  // candidate lists: boundary bins, this CTA's counts, the cluster's offsets and totals, and the
+  // thresholds and masses found on the gathered lists
+  int lD[2];
+  int lnum[2];
+  int loff[2][kMaxCluster];
+  int ltot[2];
+  int lth[2];
+  uint32_t lkey[2];
+  float lmass[2];
 };
 
 struct FPos {
@@ -275,6 +296,98 @@ __device__ void decide(FSel& S, const unsigned* gc, const float* gm, bool count_
       S.above = am;
     }
     S.tau = tau;
+  }
+}
+
+// A value below which every logit has a value bin below L: vbin is non-decreasing in z and the
+// value is checked with vbin itself, so skipping the logits below it skips no logit of bin L or
+// above. -inf when no such value is found (nothing is skipped).
+__device__ __forceinline__ float cut_below(float M, float k, int L) {
+  const float zc = M - static_cast<float>(257 - L) / (k * kBinsPerLog2);
+  return (zc == zc && vbin(zc, M, k) < L) ? zc : -INFINITY;
+}
+
+// The value bin holding the need-th largest logit, from the cluster's counts (one warp; lane l owns
+// the bins 255 - 8l .. 248 - 8l); -1 when the counted bins hold fewer than need logits.
+__device__ int boundary_bin(const unsigned* gc, unsigned need, int lane) {
+  const int base = 255 - 8 * lane;
+  unsigned c[8];
+  unsigned cl = 0u;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = gc[base - j];
+    cl += c[j];
+  }
+  const unsigned ci = warp_incl_scan_u(cl, lane);
+  const unsigned hit = __ballot_sync(kFull, ci >= need);
+  if (!hit) return -1;
+  const int owner = __ffs(hit) - 1;
+  int D = 0;
+  if (lane == owner) {
+    unsigned cum = ci - cl;
+    bool found = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (!found) {
+        cum += c[j];
+        if (cum >= need) {
+          D = base - j;
+          found = true;
+        }
+      }
+    }
+  }
+  return __shfl_sync(kFull, D, owner);
+}
+
+// One selection (count mode: top-k; else top-p) by one warp over a row's gathered candidates: the
+// levels and decisions of the chunk-wide selection, on histograms of the list's entries. Every
+// candidate of the selection (every logit at or above the lower bound (lbD0, lbkey) that can be
+// kept) must be on the list.
+template <bool BF16, int KB>
+__device__ void list_select(FSel& S, const float* zl, int n, float M, float k, unsigned* hc,
+                            float* hm, bool count_mode, unsigned need, float topp, int lbD0,
+                            uint32_t lbkey, int lane) {
+  if (lane == 0) {
+    S.act = 1;
+    S.lvl = 0;
+    S.D0 = 0;
+    S.pre = 0u;
+    S.need = need;
+    S.above = 0.0f;
+    S.tau = 0.0f;
+    S.lbD0 = lbD0;
+    S.lbkey = lbkey;
+  }
+  __syncwarp();
+  while (S.act) {
+    for (int j = lane; j < kBins; j += 32) {
+      hc[j] = 0u;
+      hm[j] = 0.0f;
+    }
+    __syncwarp();
+    const int lvl = S.lvl, D0 = S.D0;
+    const uint32_t pre = S.pre;
+    const int sh = KB - 8 * lvl;
+    for (int e = lane; e < n; e += 32) {
+      const float z = zl[e];
+      const int vb = vbin(z, M, k);
+      if (lvl == 0 ? vb < lbD0 : vb != D0) continue;
+      const uint32_t key = okey<BF16>(z);
+      bool cand = vb != lbD0 || key >= lbkey;
+      int digit = vb;
+      if (lvl > 0) {
+        cand = cand && (lvl == 1 || (key >> (sh + 8)) == pre);
+        digit = static_cast<int>((key >> sh) & 255u);
+      }
+      if (cand) {
+        atomicAdd(hc + digit, 1u);
+        atomicAdd(hm + digit, ex2((z - M) * k));
+      }
+    }
+    __syncwarp();
+    decide<KB>(S, hc, hm, count_mode, topp, lane);
+    __syncwarp();
   }
 }
 
@@ -489,6 +602,281 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
     float Sk[2] = {sm.bc[1], sm.bc[3]};          // mass of the kept set, relative to exp2(M k)
     const bool bad = sm.bi[0] != 0;
     __syncthreads();
+
+    // ---- L: a top-k position on short lists of candidates ----
+    // H counts the value bins from kLowBin up; the cluster's counts give each row's boundary bin D
+    // (the bin of the k-th largest logit). C writes every logit of bin D or above into this CTA's
+    // list of the row (the top-k set, and so the top-p set on it, lies inside). When every list
+    // fits, rank 0 gathers them in index order and finishes the position from them alone; the other
+    // CTAs go on to their next position. Otherwise the chunk-wide passes below run.
+    if (kon && !bad) {
+      const uint32_t hpar = ex & 1;
+      unsigned* whc = reinterpret_cast<unsigned*>(dyn + 2 * kFRowBytes) + warp * 2 * kBins;
+      for (int j = lane; j < 2 * kBins; j += 32) whc[j] = 0u;
+      __syncwarp();
+      for (int r = 0; r < nrows; ++r) {
+        const uint4* src = r == 0 ? dt : dd;
+        const float Mr = M[r];
+        const float zc = cut_below(Mr, k, kLowBin);
+        unsigned* hc = whc + r * kBins;
+        for (int u = tid; u < cu; u += kFT) {
+          const uint4 v = src[u];
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float z = vec_get<BF16>(v, e);
+            if (z >= zc) {
+              const int vb = vbin(z, Mr, k);
+              if (vb >= kLowBin) atomicAdd(hc + vb, 1u);
+            }
+          }
+        }
+      }
+      __syncthreads();
+      {
+        const unsigned* ahc = reinterpret_cast<const unsigned*>(dyn + 2 * kFRowBytes);
+        for (int j = tid; j < 2 * kBins; j += kFT) {
+          unsigned c = 0u;
+          if (j / kBins < nrows) {
+#pragma unroll 4
+            for (int w = 0; w < kFW; ++w) c += ahc[w * 2 * kBins + j];
+          }
+          (&sm.hc[hpar][0][0])[j] = c;
+        }
+      }
+      publish();
+      for (int j = tid; j < 2 * kBins; j += kFT) {
+        unsigned c = 0u;
+        if (j / kBins < nrows && j % kBins >= kLowBin) {
+          const uint32_t ac = smem_addr(&sm.hc[hpar][0][0] + j);
+          int cq[kMaxCluster];
+#pragma unroll
+          for (int q = 0; q < kMaxCluster; ++q)
+            if (q < C) cq[q] = ld_cluster_s32(map_to_rank(ac, static_cast<uint32_t>(q)));
+#pragma unroll
+          for (int q = 0; q < kMaxCluster; ++q)
+            if (q < C) c += static_cast<unsigned>(cq[q]);
+        }
+        (&sm.gc[0][0])[j] = c;
+      }
+      __syncthreads();
+      if (warp < nrows) {
+        const int D = boundary_bin(sm.gc[warp], static_cast<unsigned>(topk), lane);
+        if (lane == 0) sm.lD[warp] = D;
+      }
+      if (tid == 0) {
+        sm.lnum[0] = 0;
+        sm.lnum[1] = 0;
+      }
+      __syncthreads();
+      const int Dr[2] = {sm.lD[0], nrows > 1 ? sm.lD[1] : kLowBin};
+      if (Dr[0] >= kLowBin && Dr[1] >= kLowBin) {
+        // this CTA's lists: target [index, z_t, z_d at that index, rank by index], draft [z_d]
+        uint32_t* li0 = reinterpret_cast<uint32_t*>(dyn + 2 * kFRowBytes);
+        float* lz0 = reinterpret_cast<float*>(li0 + kLCap);
+        float* lw0 = lz0 + kLCap;
+        int* lr0 = reinterpret_cast<int*>(lw0 + kLCap);
+        float* lz1 = reinterpret_cast<float*>(lr0 + kLCap);
+        // the gathered lists (rank 0)
+        uint32_t* mi0 = reinterpret_cast<uint32_t*>(lz1 + kLCap);
+        float* mz0 = reinterpret_cast<float*>(mi0 + kLCap);
+        float* mw0 = mz0 + kLCap;
+        float* mz1 = mw0 + kLCap;
+        for (int r = 0; r < nrows; ++r) {
+          const uint4* src = r == 0 ? dt : dd;
+          const float Mr = M[r];
+          const int D = Dr[r];
+          const float zc = cut_below(Mr, k, D);
+          for (int u = tid; u < cu; u += kFT) {
+            const uint4 v = src[u];
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const float z = vec_get<BF16>(v, e);
+              if (z >= zc && vbin(z, Mr, k) >= D) {
+                const int slot = atomicAdd(&sm.lnum[r], 1);
+                if (slot < kLCap) {
+                  if (r == 0) {
+                    li0[slot] = static_cast<uint32_t>((u0 + u) * E + e);
+                    lz0[slot] = z;
+                    lw0[slot] = p.two ? vec_get<BF16>(dd[u], e) : 0.0f;
+                  } else {
+                    lz1[slot] = z;
+                  }
+                }
+              }
+            }
+          }
+        }
+        __syncthreads();
+        {
+          const int n0 = min(sm.lnum[0], kLCap);
+          for (int e = tid; e < n0; e += kFT) {
+            const uint32_t ie = li0[e];
+            int rk = 0;
+            for (int j = 0; j < n0; ++j) rk += li0[j] < ie ? 1 : 0;
+            lr0[e] = rk;
+          }
+        }
+        if (tid == 0) {
+          const uint32_t par = ex & 1;
+          sm.xrec[par][0] = __int_as_float(sm.lnum[0]);
+          sm.xrec[par][1] = __int_as_float(nrows > 1 ? sm.lnum[1] : 0);
+        }
+        const uint32_t lpar = publish();
+        if (warp == 0) {
+          const int c0 = lane < C ? __float_as_int(peer(lpar, 0, lane)) : 0;
+          const int c1 = lane < C ? __float_as_int(peer(lpar, 1, lane)) : 0;
+          int i0 = c0, i1 = c1;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
+            if (lane >= o) {
+              i0 += y0;
+              i1 += y1;
+            }
+          }
+          if (lane < C) {
+            sm.loff[0][lane] = i0 - c0;
+            sm.loff[1][lane] = i1 - c1;
+          }
+          if (lane == 31) {
+            sm.ltot[0] = i0;
+            sm.ltot[1] = i1;
+          }
+        }
+        __syncthreads();
+        const int N0 = sm.ltot[0], N1 = sm.ltot[1];
+        if (N0 <= kLCap && N1 <= kLCap) {
+          if (rank != 0) continue;
+          // gather: CTA q's target entries go to loff[q] + their rank by index (chunks are in index
+          // order by rank, so the list is in index order); draft entries in any order
+          for (int j = tid; j < N0; j += kFT) {
+            int q = 0;
+            while (q + 1 < C && j >= sm.loff[0][q + 1]) ++q;
+            const int e = j - sm.loff[0][q];
+            const uint32_t qq = static_cast<uint32_t>(q);
+            const int dst = sm.loff[0][q] + ld_cluster_s32(map_to_rank(smem_addr(lr0 + e), qq));
+            mi0[dst] = static_cast<uint32_t>(ld_cluster_s32(map_to_rank(smem_addr(li0 + e), qq)));
+            mz0[dst] = ld_cluster_f32(map_to_rank(smem_addr(lz0 + e), qq));
+            mw0[dst] = ld_cluster_f32(map_to_rank(smem_addr(lw0 + e), qq));
+          }
+          for (int j = tid; j < N1; j += kFT) {
+            int q = 0;
+            while (q + 1 < C && j >= sm.loff[1][q + 1]) ++q;
+            mz1[j] = ld_cluster_f32(map_to_rank(smem_addr(lz1 + (j - sm.loff[1][q])),
+                                                static_cast<uint32_t>(q)));
+          }
+          __syncthreads();
+          // K, P on the gathered lists: warp r selects row r
+          if (warp < nrows) {
+            FSel& S = sm.sel[warp];
+            const float* zl = warp == 0 ? mz0 : mz1;
+            const int nl = warp == 0 ? N0 : N1;
+            const float Mr = M[warp];
+            list_select<BF16, KB>(S, zl, nl, Mr, k, sm.gc[warp], sm.gm[warp], true,
+                                  static_cast<unsigned>(topk), topp, 0, 0u, lane);
+            int tD = S.thD0;
+            uint32_t tK = S.thkey;
+            if (pon) {
+              list_select<BF16, KB>(S, zl, nl, Mr, k, sm.gc[warp], sm.gm[warp], false,
+                                    static_cast<unsigned>(topk), topp, tD, tK, lane);
+              if (S.thD0 > tD || (S.thD0 == tD && S.thkey > tK)) {
+                tD = S.thD0;
+                tK = S.thkey;
+              }
+            }
+            if (lane == 0) {
+              sm.lth[warp] = tD;
+              sm.lkey[warp] = tK;
+              sm.lmass[warp] = S.mass;
+            }
+          }
+          __syncthreads();
+          // V, D on the gathered target list (one warp; lane l takes a contiguous run of entries)
+          if (warp == 0) {
+            const int t0 = sm.lth[0], t1 = sm.lth[1];
+            const uint32_t k0 = sm.lkey[0], k1 = sm.lkey[1];
+            const float lt = -log2f(sm.lmass[0]);
+            const float ld = p.two ? -log2f(sm.lmass[1]) : 0.0f;
+            auto wt_l = [&](float z) -> float {
+              return at_or_above(vbin(z, M[0], k), okey<BF16>(z), t0, k0)
+                         ? ex2(fmaf(z - M[0], k, lt)) : 0.0f;
+            };
+            auto wd_l = [&](float z) -> float {
+              return at_or_above(vbin(z, M[1], k), okey<BF16>(z), t1, k1)
+                         ? ex2(fmaf(z - M[1], k, ld)) : 0.0f;
+            };
+            float px = 0.0f, qx = 0.0f, acc = 1.0f;
+            if (p.two) {
+              px = wt_l(load_logit<BF16>(rowt, x));
+              qx = wd_l(load_logit<BF16>(rowd, x));
+              const float ratio = (qx > 0.0f) ? fminf(1.0f, px / qx) : 1.0f;
+              acc = __ldg(P.uniforms + (size_t)p.b * (G + 2) + p.i) < ratio ? 1.0f : 0.0f;
+            }
+            const int run = (N0 + 31) / 32;
+            const int e0 = min(lane * run, N0), e1 = min(e0 + run, N0);
+            float sp = 0.0f, sw = 0.0f;
+            int lastp = -1, lastw = -1;
+            for (int e = e0; e < e1; ++e) {
+              const float wt = wt_l(mz0[e]);
+              sp += wt;
+              if (wt > 0.0f) lastp = e;
+              if (p.two) {
+                const float w = fmaxf(wt - wd_l(mw0[e]), 0.0f);
+                sw += w;
+                if (w > 0.0f) lastw = e;
+              }
+            }
+            const float ip = warp_incl_scan(sp, lane), iw = warp_incl_scan(sw, lane);
+            const float Pt = __shfl_sync(kFull, ip, 31), Wt = __shfl_sync(kFull, iw, 31);
+            const float alpha = p.two ? fminf(1.0f, fmaxf(0.0f, 1.0f - Wt)) : 0.0f;
+            if (p.two && acc != 0.0f) {
+              finish_position(P, p.b, p.i, p.gb, -1, kFlagAccept, alpha, px, qx, lane);
+            } else {
+              // the residual (rejection), p~ when the residual has no mass, or the bonus draw
+              const bool resid = p.two && Wt > 0.0f;
+              const float* ur = P.uniforms + (size_t)p.b * (G + 2);
+              const float uu = p.two ? __ldg(ur + G) : __ldg(ur + G + 1);
+              const float t = uu * (resid ? Wt : Pt);
+              const float ts = resid ? sw : sp, incl = resid ? iw : ip;
+              float excl = __shfl_up_sync(kFull, incl, 1);
+              if (lane == 0) excl = 0.0f;
+              const unsigned cm = __ballot_sync(kFull, ts > 0.0f && incl > t);
+              int pick;
+              if (cm) {
+                const int wl = __ffs(cm) - 1;
+                int pk = -1;
+                if (lane == wl) {
+                  float c = excl;
+                  int lp = -1;
+                  for (int e = e0; e < e1 && pk < 0; ++e) {
+                    const float wt = wt_l(mz0[e]);
+                    const float w = resid ? fmaxf(wt - wd_l(mw0[e]), 0.0f) : wt;
+                    if (w > 0.0f) {
+                      lp = e;
+                      c += w;
+                      if (c > t) pk = e;
+                    }
+                  }
+                  if (pk < 0) pk = lp;
+                }
+                pick = __shfl_sync(kFull, pk, wl);
+              } else {
+                // rounding left the running sum at or below t: the last entry with weight
+                int lj = resid ? lastw : lastp;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lj = max(lj, __shfl_xor_sync(kFull, lj, o));
+                pick = lj;
+              }
+              const int tok = pick >= 0 ? static_cast<int>(mi0[pick]) : -1;
+              finish_position(P, p.b, p.i, p.gb, tok,
+                              (tok < 0 ? kFlagBad : 0) | (p.two ? 0 : kFlagAccept), alpha, px, qx,
+                              lane);
+            }
+          }
+          continue;
+        }
+      }
+    }
 
     // ---- K, P: the thresholds ----
     int thD0[2] = {0, 0};

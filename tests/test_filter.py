@@ -300,6 +300,48 @@ def test_gpu_filtered_ties_and_degenerate_rows(sv, dtype):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("dtype,V", [("bf16", 100000), ("f32", 40000)])
+def test_gpu_filtered_candidate_lists(sv, dtype, V):
+    """Top-k rows whose candidates (every logit in the value bin of the k-th largest or above) are
+    gathered into one list: a list of exactly 1024 entries (the capacity) spread over the chunks and
+    held by the last chunk alone, 1025 entries (too many: the chunk-wide selection), a k-th largest
+    far below the max (below the counted bins), top-k with top-p, and a bonus-only row."""
+    B, G = 8, 3
+    rng = np.random.default_rng(V)
+    zt = (rng.standard_normal((B, G + 1, V)) * 2.0).astype(np.float32)
+    zd = (zt[:, :G] + rng.standard_normal((B, G, V)).astype(np.float32) * 0.8).astype(np.float32)
+    T = np.ones(B, np.float32)
+    n = np.full(B, G, np.int32)
+    top_k = np.array([20, 5, 5, 5, 10, 100, 7, 50], np.int32)
+    top_p = np.array([1.0, 1.0, 1.0, 0.9, 1.0, 0.9, 1.0, 0.95], np.float32)
+    spread = rng.choice(V, 1025, replace=False)
+    zt[1, :, spread[:1024]] = 12.0          # 1024 ties at the max, every chunk
+    zd[1, :, spread[:1024]] = 12.0
+    zt[2, :, spread] = 12.0                 # 1025 ties
+    zd[2, :, spread] = 12.0
+    zt[3, :, V - 1024:] = 12.0              # 1024 ties, all in the last chunk
+    zd[3, :, V - 1024:] = 12.0
+    zt[4] = -40.0                           # three logits at the max, the rest 57 log2 units down
+    zd[4] = -40.0
+    zt[4, :, [3, V // 2, V - 5]] = 0.0
+    zd[4, :, [3, V // 2, V - 5]] = 0.0
+    n[6] = 0                                # the bonus position only
+    if dtype == "bf16":
+        zt, zd = bf16_round(zt), bf16_round(zd)
+    u = rng.random((B, G + 2), dtype=np.float32)
+    x = np.full((B, G), -1, np.int32)
+    for b in range(B):
+        for i in range(n[b]):
+            q, _ = filtered_softmax(zd[b, i], T[b], int(top_k[b]), np.float64(top_p[b]))
+            x[b, i] = inverse_cdf(q, rng.random())
+        zt[b, n[b] + 1:] = np.nan
+        zd[b, n[b]:] = np.nan
+    gpu = run_filtered(sv, zt, zd, x, n, T, u, top_k, top_p, dtype)
+    rep, skipped = check_filtered(zt, zd, x, n, T, u, top_k, top_p, gpu)
+    assert skipped <= 2, skipped
+
+
+@pytest.mark.gpu
 def test_gpu_filtered_row_errors(sv):
     B, G, V = 6, 2, 2048
     zt, zd, x, n, T, u, top_k, top_p = filter_batch(B, G, V, "f32", seed=8, greedy_frac=0.0)
