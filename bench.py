@@ -378,20 +378,36 @@ def run_gpu(args):
     e2e = None
     if not args.no_e2e:
         host = {k: v.cpu().pin_memory() for k, v in t.items()}
-        dev_in = {k: torch.empty_like(v) for k, v in t.items()}
         h_tok = torch.empty((B, G + 1), dtype=torch.int32).pin_memory()
         h_num = torch.empty((B,), dtype=torch.int32).pin_memory()
         h_alpha = torch.empty((B, G), dtype=torch.float32).pin_memory()
-        bi = sum(v.numel() * v.element_size() for v in host.values())
         bo = sum(v.numel() * v.element_size() for v in (h_tok, h_num, h_alpha))
+        if args.filter or args.onehot:
+            # every input tensor copied in whole, then the device call
+            dev_in = {k: torch.empty_like(v) for k, v in t.items()}
+            bi = sum(v.numel() * v.element_size() for v in host.values())
+            e2e_path = "every input copied in whole, then the device call"
 
-        def e2e_step():
-            for k in host:
-                dev_in[k].copy_(host[k], non_blocking=True)
-            call(dev_in)
-            h_tok.copy_(out_tokens, non_blocking=True)
-            h_num.copy_(out_num, non_blocking=True)
-            h_alpha.copy_(out_alpha, non_blocking=True)
+            def e2e_step():
+                for k in host:
+                    dev_in[k].copy_(host[k], non_blocking=True)
+                call(dev_in)
+                h_tok.copy_(out_tokens, non_blocking=True)
+                h_num.copy_(out_num, non_blocking=True)
+                h_alpha.copy_(out_alpha, non_blocking=True)
+        else:
+            # the host-buffer entry point: only the logit rows the rule reads are copied in
+            dev_in = torch.empty(sv.spec_verify_staging_size(B, G, V, dcode), dtype=torch.uint8,
+                                 device=dev)
+            bi = sv.spec_verify_staged_h2d_bytes(host["draft_len"], host["temperature"], B, G, V,
+                                                 dcode)
+            e2e_path = "spec_verify_staged: host buffers, only the rows the rule reads copied in"
+
+            def e2e_step():
+                sv.spec_verify_staged(host["target_logits"], host["draft_logits"],
+                                      host["draft_tokens"], host["draft_len"],
+                                      host["temperature"], host["uniforms"], h_tok, h_num,
+                                      h_alpha, dev_in, ws, stream)
 
         for _ in range(2):
             e2e_step()
@@ -407,7 +423,7 @@ def run_gpu(args):
         ms_e2e, _ = job_totals(e0.elapsed_time(e1) / n_e2e, positions, dev)
         e2e = {"value": positions_all / (ms_e2e * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
-               "ms_per_step": ms_e2e, "steps": n_e2e}
+               "ms_per_step": ms_e2e, "steps": n_e2e, "path": e2e_path}
         del host, dev_in
 
     cpu = None

@@ -254,6 +254,46 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
                         float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                         void* cuda_stream);
 
+/* spec_verify_ex from host buffers, copying in only what the rule reads. The pages have no
+ * counterpart: this is the host side of a serving step whose logits sit in host memory.
+ *
+ * The rule reads target rows 0..gamma_b of row b and, for a sampled row (temperature not exactly
+ * 0), draft rows 0..gamma_b - 1 ([R] "Speculative decoding", rayaq.ca ml-models -- Mechanics, One
+ * round, steps 3-5; The greedy case: a greedy row compares with the target's argmax only). So the
+ * call enqueues on `cuda_stream`, in this order: host-to-device copies of draft_tokens, draft_len,
+ * temperature and uniforms; one copy per run of contiguous logit rows that the rule reads (runs of
+ * consecutive rows b merge when row b has gamma_b = gamma_max); spec_verify_ex on the staged copies
+ * (p and q of the drafts are not returned); device-to-host copies of out_tokens, out_num_emitted and
+ * out_alpha. Padding rows are never copied, and never read by the kernels.
+ *
+ * h_*: host buffers in the layouts of spec_verify_ex (h_draft_len may be NULL = all gamma_max;
+ * h_out_alpha may be NULL; with gamma_max = 0, h_draft_logits and h_draft_tokens may be NULL). The call reads h_draft_len and
+ * h_temperature on the host before it returns; every h_* buffer must stay unchanged (inputs) and
+ * untouched (outputs) until `cuda_stream` has been synchronised. Page-locked host memory makes the
+ * copies asynchronous; pageable memory also works, at the copy speed of the driver's staging.
+ * A row whose host draft_len lies outside [0, gamma_max] has no logits copied; the kernel marks
+ * it as a row error from the staged copy of draft_len.
+ * staging: caller-owned device memory of at least spec_verify_staging_size(B, gamma_max, V, dtype)
+ * bytes, 256-byte aligned; it holds the staged inputs and outputs (its contents need no setup).
+ * workspace: as in spec_verify_ex. h2d_bytes (may be NULL): set to the host-to-device bytes
+ * enqueued. Errors: this call's own checks (dtype, sizes, NULL pointers, a staging buffer that is
+ * not 256-byte aligned or too short, a workspace too short) return a status and enqueue nothing.
+ * A status returned by the verification step (the checks of spec_verify_ex that concern the device
+ * and the kernels' limits) or SV_ERR_CUDA from a failed copy comes after the input copies were
+ * enqueued; the work enqueued before it may still run. */
+size_t spec_verify_staging_size(int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
+int spec_verify_staged(const void* h_target_logits, const void* h_draft_logits,
+                       const int32_t* h_draft_tokens, const int32_t* h_draft_len,
+                       const float* h_temperature, const float* h_uniforms,
+                       int32_t* h_out_tokens, int32_t* h_out_num_emitted, float* h_out_alpha,
+                       int32_t B, int32_t gamma_max, int32_t V, int32_t dtype, void* staging,
+                       size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                       size_t* h2d_bytes, void* cuda_stream);
+/* The host-to-device bytes spec_verify_staged enqueues for these host draft lengths and
+ * temperatures (host arrays; h_draft_len may be NULL); 0 for invalid sizes. Host code only. */
+size_t spec_verify_staged_h2d_bytes(const int32_t* h_draft_len, const float* h_temperature,
+                                    int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
+
 /* Reads the workspace's sticky status word into *status_out after synchronising `cuda_stream`
  * (B and gamma_max as in the call that used the workspace). 0 means every call so far completed
  * its protocol. A nonzero value means a kernel-internal wait gave up (every wait inside the

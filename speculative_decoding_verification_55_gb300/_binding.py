@@ -77,6 +77,14 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_status_string.restype = ctypes.c_char_p
             L.spec_verify_version.argtypes = []
             L.spec_verify_version.restype = ctypes.c_int
+            L.spec_verify_staging_size.argtypes = [i32, i32, i32, i32]
+            L.spec_verify_staging_size.restype = ctypes.c_size_t
+            L.spec_verify_staged_h2d_bytes.argtypes = [vp, vp, i32, i32, i32, i32]
+            L.spec_verify_staged_h2d_bytes.restype = ctypes.c_size_t
+            L.spec_verify_staged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                                             vp, ctypes.c_size_t, vp, ctypes.c_size_t,
+                                             ctypes.POINTER(ctypes.c_size_t), vp]
+            L.spec_verify_staged.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -170,6 +178,90 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, tempera
         _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_ex")
+
+
+def spec_verify_staging_size(B: int, gamma_max: int, V: int, dtype: int) -> int:
+    return int(lib().spec_verify_staging_size(B, gamma_max, V, dtype))
+
+
+def _host_ptr(a):
+    """Address of a host buffer: a CPU torch tensor or a contiguous numpy array (None -> NULL)."""
+    if a is None:
+        return None
+    if hasattr(a, "data_ptr"):
+        if a.is_cuda:
+            raise ValueError("expected a host (CPU) buffer")
+        return a.data_ptr()
+    if not a.flags["C_CONTIGUOUS"]:
+        raise ValueError("host arrays must be contiguous")
+    return a.ctypes.data
+
+
+def spec_verify_staged_h2d_bytes(draft_len, temperature, B: int, gamma_max: int, V: int,
+                                 dtype: int) -> int:
+    """Host-to-device bytes spec_verify_staged enqueues for these host draft lengths (int32, or
+    None) and temperatures (float32)."""
+    return int(lib().spec_verify_staged_h2d_bytes(_host_ptr(draft_len), _host_ptr(temperature),
+                                                  B, gamma_max, V, dtype))
+
+
+def spec_verify_staged(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                       out_tokens, out_num_emitted, out_alpha, staging, workspace,
+                       stream=None) -> int:
+    """Calls the C ABI spec_verify_staged: host (CPU, ideally pinned) torch tensors in and out,
+    device staging and workspace buffers. Returns the host-to-device bytes enqueued."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    cpu = torch.device("cpu")
+    _check(target_logits, "target_logits", device=cpu)
+    _check(draft_logits, "draft_logits", dtype=target_logits.dtype, shape=(B, G, V), device=cpu)
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, G), cpu)
+    _check(draft_len, "draft_len", torch.int32, (B,), cpu)
+    _check(temperature, "temperature", torch.float32, (B,), cpu)
+    _check(uniforms, "uniforms", torch.float32, (B, G + 2), cpu)
+    _check(out_tokens, "out_tokens", torch.int32, (B, G + 1), cpu)
+    _check(out_num_emitted, "out_num_emitted", torch.int32, (B,), cpu)
+    _check(out_alpha, "out_alpha", torch.float32, (B, G), cpu)
+    dev = staging.device
+    _check(workspace, "workspace", device=dev)
+    n = ctypes.c_size_t(0)
+    st = lib().spec_verify_staged(
+        _host_ptr(target_logits), _host_ptr(draft_logits), _host_ptr(draft_tokens),
+        _host_ptr(draft_len), _host_ptr(temperature), _host_ptr(uniforms), _host_ptr(out_tokens),
+        _host_ptr(out_num_emitted), _host_ptr(out_alpha), B, G, V, _dtype_code(target_logits),
+        _ptr(staging), staging.numel() * staging.element_size(), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), ctypes.byref(n), _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_staged")
+    return int(n.value)
+
+
+_staging_cache = {}
+
+
+def verify_staged(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                  device=None, stream=None):
+    """spec_verify_staged with pinned host outputs and a cached device staging buffer and
+    workspace. Returns (out_tokens, out_num_emitted, out_alpha, h2d_bytes); the outputs are valid
+    once the stream has been synchronised."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    device = torch.device(device or "cuda")
+    dt = _dtype_code(target_logits)
+    key = (str(device), _stream_handle(stream, device), B, G, V, dt)
+    if key not in _staging_cache:
+        _staging_cache[key] = torch.empty(spec_verify_staging_size(B, G, V, dt), dtype=torch.uint8,
+                                          device=device)
+    ws = workspace_for(B, G, V, dt, device, stream)
+    out_tokens = torch.empty((B, G1), dtype=torch.int32).pin_memory()
+    out_num = torch.empty((B,), dtype=torch.int32).pin_memory()
+    out_alpha = torch.empty((B, G), dtype=torch.float32).pin_memory()
+    n = spec_verify_staged(target_logits, draft_logits, draft_tokens, draft_len, temperature,
+                           uniforms, out_tokens, out_num, out_alpha, _staging_cache[key], ws,
+                           stream)
+    return out_tokens, out_num, out_alpha, n
 
 
 def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, draft_len, temperature,
