@@ -49,13 +49,17 @@ constexpr int kHistBytes = kFW * 2 * kBins * 8;
 constexpr int kFDynBytes = 2 * kFRowBytes + kHistBytes;
 constexpr int kCopyPiece = 16384;               // bytes per bulk copy
 constexpr float kBinsPerLog2 = 8.0f;            // level-0 resolution
-// Top-k rows: the count pass counts the value bins from kLowBin up (logits within 24 units of log2
-// probability of the max); a candidate list holds at most kLCap logits of a row, per CTA and for
-// the whole cluster. The target list's four arrays and the draft list's one sit where the per-warp
-// histograms were, the rank-0 gathered lists after them.
+// Top-k rows: the count pass counts the value bins from kHighBin up, and from kLowBin up (logits
+// within 24 units of log2 probability of the max) when fewer than k logits lie that high. A
+// candidate list holds at most kLCap logits of a row, per CTA and for the whole cluster. A CTA's
+// lists (the target list's four arrays, the draft list's one) sit in the upper half of the
+// histogram area, which the count-only passes do not use; rank 0's gathered lists in the lower.
 constexpr int kLowBin = 64;
+constexpr int kHighBin = 192;                   // within 8 units of log2 probability of the max
 constexpr int kLCap = 1024;
-static_assert(9 * kLCap * 4 <= kHistBytes, "candidate lists exceed the histogram area");
+static_assert(kFW * 2 * kBins * 4 <= kHistBytes / 2, "count histograms exceed half the area");
+static_assert(5 * kLCap * 4 <= kHistBytes / 2 && 4 * kLCap * 4 <= kHistBytes / 2,
+              "candidate lists exceed half the histogram area");
 
 enum : unsigned { kStatusTimeout = 1u };
 
@@ -340,34 +344,22 @@ __device__ int boundary_bin(const unsigned* gc, unsigned need, int lane) {
   return __shfl_sync(kFull, D, owner);
 }
 
-// One selection (count mode: top-k; else top-p) by one warp over a row's gathered candidates: the
-// levels and decisions of the chunk-wide selection, on histograms of the list's entries. Every
-// candidate of the selection (every logit at or above the lower bound (lbD0, lbkey) that can be
-// kept) must be on the list.
+// The remaining levels of a selection (count mode: top-k; else top-p), from the state in S, by one
+// warp over a row's gathered candidates: the levels and decisions of the chunk-wide selection, on
+// histograms of the list's entries. Every candidate the remaining levels look at (every logit at
+// or above the lower bound (lbD0, lbkey), in the level-0 bin D0 once level 0 is decided) must be on
+// the list; other entries are harmless.
 template <bool BF16, int KB>
-__device__ void list_select(FSel& S, const float* zl, int n, float M, float k, unsigned* hc,
-                            float* hm, bool count_mode, unsigned need, float topp, int lbD0,
-                            uint32_t lbkey, int lane) {
-  if (lane == 0) {
-    S.act = 1;
-    S.lvl = 0;
-    S.D0 = 0;
-    S.pre = 0u;
-    S.need = need;
-    S.above = 0.0f;
-    S.tau = 0.0f;
-    S.lbD0 = lbD0;
-    S.lbkey = lbkey;
-  }
-  __syncwarp();
+__device__ void list_refine(FSel& S, const float* zl, int n, float M, float k, unsigned* hc,
+                            float* hm, bool count_mode, float topp, int lane) {
   while (S.act) {
     for (int j = lane; j < kBins; j += 32) {
       hc[j] = 0u;
       hm[j] = 0.0f;
     }
     __syncwarp();
-    const int lvl = S.lvl, D0 = S.D0;
-    const uint32_t pre = S.pre;
+    const int lvl = S.lvl, D0 = S.D0, lbD0 = S.lbD0;
+    const uint32_t pre = S.pre, lbkey = S.lbkey;
     const int sh = KB - 8 * lvl;
     for (int e = lane; e < n; e += 32) {
       const float z = zl[e];
@@ -389,6 +381,27 @@ __device__ void list_select(FSel& S, const float* zl, int n, float M, float k, u
     decide<KB>(S, hc, hm, count_mode, topp, lane);
     __syncwarp();
   }
+}
+
+// A whole selection on a gathered list: the state of level 0 with the lower bound (lbD0, lbkey)
+// (a top-p selection on the top-k set takes the top-k threshold), then list_refine.
+template <bool BF16, int KB>
+__device__ void list_select(FSel& S, const float* zl, int n, float M, float k, unsigned* hc,
+                            float* hm, bool count_mode, unsigned need, float topp, int lbD0,
+                            uint32_t lbkey, int lane) {
+  if (lane == 0) {
+    S.act = 1;
+    S.lvl = 0;
+    S.D0 = 0;
+    S.pre = 0u;
+    S.need = need;
+    S.above = 0.0f;
+    S.tau = 0.0f;
+    S.lbD0 = lbD0;
+    S.lbkey = lbkey;
+  }
+  __syncwarp();
+  list_refine<BF16, KB>(S, zl, n, M, k, hc, hm, count_mode, topp, lane);
 }
 
 template <bool BF16>
@@ -434,6 +447,25 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
     return ld_cluster_f32(map_to_rank(smem_addr(&sm.xrec[par][field]), static_cast<uint32_t>(r)));
   };
 
+  // Bulk copies of this CTA's chunk of position q's row(s) (thread 0), completing on sm.bar.
+  auto issue_copy = [&](const FPos& q) {
+    const int nr = q.two ? 2 : 1;
+    const uint32_t bytes = static_cast<uint32_t>(cu) * 16;
+    mbar_arrive_expect_tx(smem_addr(&sm.bar), bytes * nr);
+    const uint64_t once = l2_policy_evict_first();
+    for (int r = 0; r < nr; ++r) {
+      const char* g = r == 0
+          ? static_cast<const char*>(P.zt) + ((size_t)q.b * G1 + q.i) * Vs * ES
+          : static_cast<const char*>(P.zd) + ((size_t)q.b * G + q.i) * Vs * ES;
+      g += static_cast<size_t>(u0) * 16;
+      const uint32_t dst = smem_addr(dyn) + r * kFRowBytes;
+      for (uint32_t off = 0; off < bytes; off += kCopyPiece)
+        bulk_g2s(dst + off, g + off, min(static_cast<uint32_t>(kCopyPiece), bytes - off),
+                 smem_addr(&sm.bar), once);
+    }
+  };
+  int pf = -1;              // thread 0: the position slot whose copies were issued ahead
+
   for (int s = cid; s < total; s += P.nclusters) {
     if (sm.stop) break;                         // set from exchanged data: the same on every CTA
     const FPos p = fclassify(P, s);
@@ -445,18 +477,10 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
     const char* rowt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES;
     const char* rowd = p.two ? static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES
                              : nullptr;
-    // ---- the chunk(s) into shared memory ----
+    // ---- the chunk(s) into shared memory (unless issued ahead) ----
     if (tid == 0) {
-      const uint32_t bytes = static_cast<uint32_t>(cu) * 16;
-      mbar_arrive_expect_tx(smem_addr(&sm.bar), bytes * nrows);
-      const uint64_t once = l2_policy_evict_first();
-      for (int r = 0; r < nrows; ++r) {
-        const char* g = (r == 0 ? rowt : rowd) + static_cast<size_t>(u0) * 16;
-        const uint32_t dst = smem_addr(dyn) + r * kFRowBytes;
-        for (uint32_t off = 0; off < bytes; off += kCopyPiece)
-          bulk_g2s(dst + off, g + off, min(static_cast<uint32_t>(kCopyPiece), bytes - off),
-                   smem_addr(&sm.bar), once);
-      }
+      if (pf != s) issue_copy(p);
+      pf = -1;
     }
     const bool landed = __syncthreads_and(mbar_wait(smem_addr(&sm.bar), npos & 1)) != 0;
     ++npos;
@@ -601,86 +625,155 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
     const float M[2] = {sm.bc[0], sm.bc[2]};
     float Sk[2] = {sm.bc[1], sm.bc[3]};          // mass of the kept set, relative to exp2(M k)
     const bool bad = sm.bi[0] != 0;
+    if (tid == 0) {
+      sm.lnum[0] = 0;
+      sm.lnum[1] = 0;
+    }
     __syncthreads();
 
-    // ---- L: a top-k position on short lists of candidates ----
-    // H counts the value bins from kLowBin up; the cluster's counts give each row's boundary bin D
-    // (the bin of the k-th largest logit). C writes every logit of bin D or above into this CTA's
-    // list of the row (the top-k set, and so the top-p set on it, lies inside). When every list
-    // fits, rank 0 gathers them in index order and finishes the position from them alone; the other
-    // CTAs go on to their next position. Otherwise the chunk-wide passes below run.
-    if (kon && !bad) {
-      const uint32_t hpar = ex & 1;
-      unsigned* whc = reinterpret_cast<unsigned*>(dyn + 2 * kFRowBytes) + warp * 2 * kBins;
-      for (int j = lane; j < 2 * kBins; j += 32) whc[j] = 0u;
-      __syncwarp();
-      for (int r = 0; r < nrows; ++r) {
-        const uint4* src = r == 0 ? dt : dd;
-        const float Mr = M[r];
-        const float zc = cut_below(Mr, k, kLowBin);
-        unsigned* hc = whc + r * kBins;
-        for (int u = tid; u < cu; u += kFT) {
-          const uint4 v = src[u];
+    // this CTA's lists: target [index, z_t, z_d at that index, rank by index], draft [z_d]; in
+    // the half of the histogram area that the count passes leave alone (they are written while
+    // the per-warp counts are live)
+    uint32_t* li0 = reinterpret_cast<uint32_t*>(dyn + 2 * kFRowBytes + kHistBytes / 2);
+    float* lz0 = reinterpret_cast<float*>(li0 + kLCap);
+    float* lw0 = lz0 + kLCap;
+    int* lr0 = reinterpret_cast<int*>(lw0 + kLCap);
+    float* lz1 = reinterpret_cast<float*>(lr0 + kLCap);
+    // the gathered lists (rank 0, written after the counts were summed)
+    uint32_t* mi0 = reinterpret_cast<uint32_t*>(dyn + 2 * kFRowBytes);
+    float* mz0 = reinterpret_cast<float*>(mi0 + kLCap);
+    float* mw0 = mz0 + kLCap;
+    float* mz1 = mw0 + kLCap;
+
+    // Warp 0: the peers' list lengths (exchange record `par`), their offsets and totals.
+    auto list_offsets = [&](uint32_t par) {
+      if (warp != 0) return;
+      const int c0 = lane < C ? __float_as_int(peer(par, 0, lane)) : 0;
+      const int c1 = lane < C ? __float_as_int(peer(par, 1, lane)) : 0;
+      int i0 = c0, i1 = c1;
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float z = vec_get<BF16>(v, e);
-            if (z >= zc) {
-              const int vb = vbin(z, Mr, k);
-              if (vb >= kLowBin) atomicAdd(hc + vb, 1u);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
+        if (lane >= o) {
+          i0 += y0;
+          i1 += y1;
+        }
+      }
+      if (lane < C) {
+        sm.loff[0][lane] = i0 - c0;
+        sm.loff[1][lane] = i1 - c1;
+      }
+      if (lane == 31) {
+        sm.ltot[0] = i0;
+        sm.ltot[1] = i1;
+      }
+    };
+    // ---- L: a top-k position on short lists of candidates ----
+    // The cluster's counts of the value bins near the max give each row's boundary bin D (the bin
+    // of the k-th largest logit): first from kHighBin up (few logits pass the prefilter), again from
+    // kLowBin up when fewer than k logits lie that high. A second pass writes every logit of bin D
+    // or above into this CTA's list of the row (the top-k set, and so the top-p set on it, lies
+    // inside). When every list fits, rank 0 gathers them in index order and finishes the position
+    // from them alone; the other CTAs go on to their next position. Otherwise the chunk-wide passes
+    // below run. (Listing every logit from kHighBin up during the first count saves the second pass
+    // and its exchange, but the longer lists cost rank 0 more than that on the benchmark rows.)
+    if (kon && !bad) {
+      // Appends logit e of vector u of row r (value z) to this CTA's list of the row.
+      auto append = [&](int r, int u, int e, float z) {
+        const int slot = atomicAdd(&sm.lnum[r], 1);
+        if (slot < kLCap) {
+          if (r == 0) {
+            li0[slot] = static_cast<uint32_t>((u0 + u) * E + e);
+            lz0[slot] = z;
+            lw0[slot] = p.two ? vec_get<BF16>(dd[u], e) : 0.0f;
+          } else {
+            lz1[slot] = z;
+          }
+        }
+      };
+      // Ranks of the target list's entries by vocabulary index.
+      auto rank_entries = [&]() {
+        const int n0 = min(sm.lnum[0], kLCap);
+        for (int e = tid; e < n0; e += kFT) {
+          const uint32_t ie = li0[e];
+          int rk = 0;
+          for (int j = 0; j < n0; ++j) rk += li0[j] < ie ? 1 : 0;
+          lr0[e] = rk;
+        }
+      };
+      // Counts the value bins from `lo` up, exchanges the counts and finds each row's boundary bin
+      // (sm.lD; -1 when the counted bins hold fewer than k logits).
+      auto count_pass = [&](int lo) {
+        const uint32_t hpar = ex & 1;
+        unsigned* whc = reinterpret_cast<unsigned*>(dyn + 2 * kFRowBytes) + warp * 2 * kBins;
+        for (int j = lane; j < 2 * kBins; j += 32) whc[j] = 0u;
+        __syncwarp();
+        for (int r = 0; r < nrows; ++r) {
+          const uint4* src = r == 0 ? dt : dd;
+          const float Mr = M[r];
+          const float zc = cut_below(Mr, k, lo);
+          unsigned* hc = whc + r * kBins;
+          for (int u = tid; u < cu; u += kFT) {
+            const uint4 v = src[u];
+            if (!(vec_max<BF16>(v) >= zc)) continue;  // one packed test for the vector's logits
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const float z = vec_get<BF16>(v, e);
+              if (z >= zc) {
+                const int vb = vbin(z, Mr, k);
+                if (vb >= lo) atomicAdd(hc + vb, 1u);
+              }
             }
           }
         }
-      }
-      __syncthreads();
-      {
-        const unsigned* ahc = reinterpret_cast<const unsigned*>(dyn + 2 * kFRowBytes);
+        __syncthreads();
+        {
+          const unsigned* ahc = reinterpret_cast<const unsigned*>(dyn + 2 * kFRowBytes);
+          for (int j = tid; j < 2 * kBins; j += kFT) {
+            unsigned c = 0u;
+            if (j / kBins < nrows) {
+#pragma unroll 4
+              for (int w = 0; w < kFW; ++w) c += ahc[w * 2 * kBins + j];
+            }
+            (&sm.hc[hpar][0][0])[j] = c;
+          }
+        }
+        publish();
         for (int j = tid; j < 2 * kBins; j += kFT) {
           unsigned c = 0u;
-          if (j / kBins < nrows) {
-#pragma unroll 4
-            for (int w = 0; w < kFW; ++w) c += ahc[w * 2 * kBins + j];
+          if (j / kBins < nrows && j % kBins >= lo) {
+            const uint32_t ac = smem_addr(&sm.hc[hpar][0][0] + j);
+            int cq[kMaxCluster];
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+              if (q < C) cq[q] = ld_cluster_s32(map_to_rank(ac, static_cast<uint32_t>(q)));
+#pragma unroll
+            for (int q = 0; q < kMaxCluster; ++q)
+              if (q < C) c += static_cast<unsigned>(cq[q]);
           }
-          (&sm.hc[hpar][0][0])[j] = c;
+          (&sm.gc[0][0])[j] = c;
         }
-      }
-      publish();
-      for (int j = tid; j < 2 * kBins; j += kFT) {
-        unsigned c = 0u;
-        if (j / kBins < nrows && j % kBins >= kLowBin) {
-          const uint32_t ac = smem_addr(&sm.hc[hpar][0][0] + j);
-          int cq[kMaxCluster];
-#pragma unroll
-          for (int q = 0; q < kMaxCluster; ++q)
-            if (q < C) cq[q] = ld_cluster_s32(map_to_rank(ac, static_cast<uint32_t>(q)));
-#pragma unroll
-          for (int q = 0; q < kMaxCluster; ++q)
-            if (q < C) c += static_cast<unsigned>(cq[q]);
+        __syncthreads();
+        if (warp < nrows) {
+          const int D = boundary_bin(sm.gc[warp], static_cast<unsigned>(topk), lane);
+          if (lane == 0) sm.lD[warp] = D;
         }
-        (&sm.gc[0][0])[j] = c;
+        if (tid == 0) {
+          sm.lnum[0] = 0;
+          sm.lnum[1] = 0;
+        }
+        __syncthreads();
+      };
+
+      bool listed = false;
+      count_pass(kHighBin);
+      int Dr[2] = {sm.lD[0], nrows > 1 ? sm.lD[1] : kHighBin};
+      if (!(Dr[0] >= kHighBin && Dr[1] >= kHighBin)) {   // cluster-wide counts: same on every CTA
+        count_pass(kLowBin);
+        Dr[0] = sm.lD[0];
+        Dr[1] = nrows > 1 ? sm.lD[1] : kLowBin;
       }
-      __syncthreads();
-      if (warp < nrows) {
-        const int D = boundary_bin(sm.gc[warp], static_cast<unsigned>(topk), lane);
-        if (lane == 0) sm.lD[warp] = D;
-      }
-      if (tid == 0) {
-        sm.lnum[0] = 0;
-        sm.lnum[1] = 0;
-      }
-      __syncthreads();
-      const int Dr[2] = {sm.lD[0], nrows > 1 ? sm.lD[1] : kLowBin};
       if (Dr[0] >= kLowBin && Dr[1] >= kLowBin) {
-        // this CTA's lists: target [index, z_t, z_d at that index, rank by index], draft [z_d]
-        uint32_t* li0 = reinterpret_cast<uint32_t*>(dyn + 2 * kFRowBytes);
-        float* lz0 = reinterpret_cast<float*>(li0 + kLCap);
-        float* lw0 = lz0 + kLCap;
-        int* lr0 = reinterpret_cast<int*>(lw0 + kLCap);
-        float* lz1 = reinterpret_cast<float*>(lr0 + kLCap);
-        // the gathered lists (rank 0)
-        uint32_t* mi0 = reinterpret_cast<uint32_t*>(lz1 + kLCap);
-        float* mz0 = reinterpret_cast<float*>(mi0 + kLCap);
-        float* mw0 = mz0 + kLCap;
-        float* mz1 = mw0 + kLCap;
         for (int r = 0; r < nrows; ++r) {
           const uint4* src = r == 0 ? dt : dd;
           const float Mr = M[r];
@@ -688,64 +781,38 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
           const float zc = cut_below(Mr, k, D);
           for (int u = tid; u < cu; u += kFT) {
             const uint4 v = src[u];
+            if (!(vec_max<BF16>(v) >= zc)) continue;
 #pragma unroll
             for (int e = 0; e < E; ++e) {
               const float z = vec_get<BF16>(v, e);
-              if (z >= zc && vbin(z, Mr, k) >= D) {
-                const int slot = atomicAdd(&sm.lnum[r], 1);
-                if (slot < kLCap) {
-                  if (r == 0) {
-                    li0[slot] = static_cast<uint32_t>((u0 + u) * E + e);
-                    lz0[slot] = z;
-                    lw0[slot] = p.two ? vec_get<BF16>(dd[u], e) : 0.0f;
-                  } else {
-                    lz1[slot] = z;
-                  }
-                }
-              }
+              if (z >= zc && vbin(z, Mr, k) >= D) append(r, u, e, z);
             }
           }
         }
         __syncthreads();
-        {
-          const int n0 = min(sm.lnum[0], kLCap);
-          for (int e = tid; e < n0; e += kFT) {
-            const uint32_t ie = li0[e];
-            int rk = 0;
-            for (int j = 0; j < n0; ++j) rk += li0[j] < ie ? 1 : 0;
-            lr0[e] = rk;
-          }
-        }
+        rank_entries();
         if (tid == 0) {
           const uint32_t par = ex & 1;
           sm.xrec[par][0] = __int_as_float(sm.lnum[0]);
           sm.xrec[par][1] = __int_as_float(nrows > 1 ? sm.lnum[1] : 0);
         }
-        const uint32_t lpar = publish();
-        if (warp == 0) {
-          const int c0 = lane < C ? __float_as_int(peer(lpar, 0, lane)) : 0;
-          const int c1 = lane < C ? __float_as_int(peer(lpar, 1, lane)) : 0;
-          int i0 = c0, i1 = c1;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y0 = __shfl_up_sync(kFull, i0, o), y1 = __shfl_up_sync(kFull, i1, o);
-            if (lane >= o) {
-              i0 += y0;
-              i1 += y1;
+        list_offsets(publish());
+        __syncthreads();
+        listed = sm.ltot[0] <= kLCap && sm.ltot[1] <= kLCap;
+      }
+      if (listed) {
+        const int N0 = sm.ltot[0], N1 = sm.ltot[1];
+        {
+          // Every list fits: this position reads no row chunk any more, so the next position's
+          // copies start now, under the gathering and rank 0's work on the lists.
+          if (tid == 0) {
+            int s2 = s + P.nclusters;
+            while (s2 < total && !fclassify(P, s2).load) s2 += P.nclusters;
+            if (s2 < total) {
+              issue_copy(fclassify(P, s2));
+              pf = s2;
             }
           }
-          if (lane < C) {
-            sm.loff[0][lane] = i0 - c0;
-            sm.loff[1][lane] = i1 - c1;
-          }
-          if (lane == 31) {
-            sm.ltot[0] = i0;
-            sm.ltot[1] = i1;
-          }
-        }
-        __syncthreads();
-        const int N0 = sm.ltot[0], N1 = sm.ltot[1];
-        if (N0 <= kLCap && N1 <= kLCap) {
           if (rank != 0) continue;
           // gather: CTA q's target entries go to loff[q] + their rank by index (chunks are in index
           // order by rank, so the list is in index order); draft entries in any order
@@ -1154,8 +1221,12 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
                       alpha, px, qx, lane);
     }
   }
-  // A copy that timed out may still land: wait for it (bounded) before this CTA can exit.
-  if (my_tmo && tid == 0) mbar_wait(smem_addr(&sm.bar), (npos - 1) & 1);
+  // A copy that timed out, or one issued ahead for a position the cluster did not reach, may still
+  // land: wait for it (bounded) before this CTA can exit.
+  if (tid == 0) {
+    if (my_tmo) mbar_wait(smem_addr(&sm.bar), (npos - 1) & 1);
+    if (pf >= 0) mbar_wait(smem_addr(&sm.bar), npos & 1);
+  }
   cluster_sync_all();        // no CTA leaves while a peer may still read its shared memory
 }
 
