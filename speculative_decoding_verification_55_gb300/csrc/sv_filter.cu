@@ -145,6 +145,36 @@ __device__ __forceinline__ bool at_or_above(int vb, uint32_t key, int D0, uint32
   return vb > D0 || (vb == D0 && key >= key0);
 }
 
+// The smallest float whose (value bin, order key) lies at or above (D0, key0). Both are
+// non-decreasing in z, so for every z <= M: (vbin(z), okey(z)) >= (D0, key0) exactly when
+// z >= the result. One warp: a 32-way search over the order of the floats (about 7 steps). The
+// threshold must keep M (every top-k and top-p set holds the row max).
+template <bool BF16>
+__device__ float kept_threshold(float M, float k, int D0, uint32_t key0, int lane) {
+  auto f2k = [](float z) -> uint32_t {
+    const uint32_t b = __float_as_uint(z);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  };
+  auto k2f = [](uint32_t q) -> float {
+    return __uint_as_float((q & 0x80000000u) ? (q & 0x7fffffffu) : ~q);
+  };
+  auto keep = [&](float z) { return at_or_above(vbin(z, M, k), okey<BF16>(z), D0, key0); };
+  if (keep(-INFINITY)) return -INFINITY;
+  uint32_t lo = f2k(-INFINITY), hi = f2k(M);    // keep(lo) false, keep(hi) true
+  while (hi - lo > 1u) {
+    const uint64_t span = hi - lo;
+    const uint32_t q = lo + static_cast<uint32_t>(span * static_cast<uint64_t>(lane + 1) / 33u);
+    const bool t = q <= lo ? false : (q >= hi ? true : keep(k2f(q)));
+    const unsigned m = __ballot_sync(kFull, t);
+    const int f = m ? __ffs(m) - 1 : 32;         // the first lane whose point is kept
+    const uint32_t qh = __shfl_sync(kFull, q, f < 32 ? f : 31);
+    const uint32_t ql = __shfl_sync(kFull, q, f > 0 ? f - 1 : 0);
+    if (f < 32) hi = qh;
+    if (f > 0) lo = ql;
+  }
+  return k2f(hi);
+}
+
 __device__ __forceinline__ float block_sum(float v, FShared& sm, int slot) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   v = warp_sum_lane0(v);
@@ -1078,11 +1108,19 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
     }
 
     // ---- V: the filtered p~ (and q~), the accept test, the chunk totals ----
-    auto kept = [&](float z, int r) -> bool {
-      if (!filt) return true;
-      const int vb = vbin(z, M[r], k);
-      return vb > thD0[r] || (vb == thD0[r] && okey<BF16>(z) >= thkey[r]);
-    };
+    // kept: (vbin, okey) at or above the row's threshold, i.e. z at or above its smallest float
+    float zth[2] = {-INFINITY, -INFINITY};
+    if (filt && !bad) {
+      if (warp < nrows) {
+        const float t = kept_threshold<BF16>(M[warp], k, warp == 0 ? thD0[0] : thD0[1],
+                                             warp == 0 ? thkey[0] : thkey[1], lane);
+        if (lane == 0) sm.bc[4 + warp] = t;
+      }
+      __syncthreads();
+      zth[0] = sm.bc[4];
+      zth[1] = sm.bc[5];
+    }
+    auto kept = [&](float z, int r) -> bool { return !filt || z >= zth[r]; };
     const float lt = -log2f(Sk[0]);              // p~(v) = exp2((z - M) k - log2 Sk) on kept logits
     const float ld = p.two ? -log2f(Sk[1]) : 0.0f;
     auto wt_of = [&](float z) -> float { return kept(z, 0) ? ex2(fmaf(z - M[0], k, lt)) : 0.0f; };
