@@ -147,8 +147,8 @@ __device__ __forceinline__ bool at_or_above(int vb, uint32_t key, int D0, uint32
 
 // The smallest float whose (value bin, order key) lies at or above (D0, key0). Both are
 // non-decreasing in z, so for every z <= M: (vbin(z), okey(z)) >= (D0, key0) exactly when
-// z >= the result. One warp: a 32-way search over the order of the floats (about 7 steps). The
-// threshold must keep M (every top-k and top-p set holds the row max).
+// z >= the result. One warp: a 32-way search over the order of the floats (about 7 steps). +inf
+// when not even M lies that high.
 template <bool BF16>
 __device__ float kept_threshold(float M, float k, int D0, uint32_t key0, int lane) {
   auto f2k = [](float z) -> uint32_t {
@@ -160,6 +160,7 @@ __device__ float kept_threshold(float M, float k, int D0, uint32_t key0, int lan
   };
   auto keep = [&](float z) { return at_or_above(vbin(z, M, k), okey<BF16>(z), D0, key0); };
   if (keep(-INFINITY)) return -INFINITY;
+  if (!keep(M)) return INFINITY;
   uint32_t lo = f2k(-INFINITY), hi = f2k(M);    // keep(lo) false, keep(hi) true
   while (hi - lo > 1u) {
     const uint64_t span = hi - lo;
@@ -173,6 +174,30 @@ __device__ float kept_threshold(float M, float k, int D0, uint32_t key0, int lan
     if (f > 0) lo = ql;
   }
   return k2f(hi);
+}
+
+// The logits a selection level looks at, as an interval [zlo, zhi) of floats (one warp): level 0
+// takes every logit at or above the lower bound (lbD0, lbkey); a deeper level takes the level-0 bin
+// D0 at or above the bound, with the key digits chosen so far. Each end is a threshold on
+// (value bin, order key), both non-decreasing in z.
+template <bool BF16, int KB>
+__device__ void level_interval(const FSel& S, float M, float k, int lane, float& zlo, float& zhi) {
+  if (S.lvl == 0) {
+    zlo = kept_threshold<BF16>(M, k, S.lbD0, S.lbkey, lane);
+    zhi = INFINITY;
+    return;
+  }
+  const int sp = KB - 8 * (S.lvl - 1);          // the digits chosen so far sit at bits >= sp
+  uint32_t klo = 0u;
+  uint64_t khi = 1ull << KB;                     // one past the largest key of the bin
+  if (S.lvl > 1) {
+    klo = S.pre << sp;
+    khi = static_cast<uint64_t>(S.pre + 1u) << sp;
+  }
+  if (S.D0 == S.lbD0 && S.lbkey > klo) klo = S.lbkey;
+  zlo = kept_threshold<BF16>(M, k, S.D0, klo, lane);
+  if (khi < (1ull << KB)) zhi = kept_threshold<BF16>(M, k, S.D0, static_cast<uint32_t>(khi), lane);
+  else zhi = S.D0 == 255 ? INFINITY : kept_threshold<BF16>(M, k, S.D0 + 1, 0u, lane);
 }
 
 __device__ __forceinline__ float block_sum(float v, FShared& sm, int slot) {
@@ -995,6 +1020,15 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
         }
         __syncthreads();
         while (sm.sel[0].act || (nrows > 1 && sm.sel[1].act)) {
+          if (warp < nrows && sm.sel[warp].act) {
+            float zlo, zhi;
+            level_interval<BF16, KB>(sm.sel[warp], warp == 0 ? M[0] : M[1], k, lane, zlo, zhi);
+            if (lane == 0) {
+              sm.bc[10 + 2 * warp] = zlo;
+              sm.bc[11 + 2 * warp] = zhi;
+            }
+          }
+          __syncthreads();
           // histograms of the active rows' candidates: per warp, then summed over the warps in order
           const uint32_t par = ex & 1;
           unsigned* whc = reinterpret_cast<unsigned*>(dyn + 2 * kFRowBytes) + warp * 2 * kBins;
@@ -1012,28 +1046,19 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
             const int sh = KB - 8 * S.lvl;
             unsigned* hc = whc + r * kBins;
             float* hm = whm + r * kBins;
-            // The value bin rules out almost every logit at the deeper levels (and, under a lower
-            // bound, at level 0); the order key is computed only for the logits it leaves.
-            const int binlo = S.lvl == 0 ? S.lbD0 : S.D0;
-            const int binhi = S.lvl == 0 ? 255 : S.D0;
+            // the level's candidates are the logits in [zlo, zhi); only they get a bin or a key
+            const float zlo = sm.bc[10 + 2 * r], zhi = sm.bc[11 + 2 * r];
             for (int u = tid; u < cu; u += kFT) {
               const uint4 v = src[u];
+              if (!(vec_max<BF16>(v) >= zlo)) continue;
 #pragma unroll
               for (int e = 0; e < E; ++e) {
                 const float z = vec_get<BF16>(v, e);
-                const int vb = vbin(z, Mr, k);
-                if (vb >= binlo && vb <= binhi) {
-                  const uint32_t key = okey<BF16>(z);
-                  bool cand = vb != S.lbD0 || key >= S.lbkey;
-                  int digit = vb;
-                  if (S.lvl > 0) {
-                    cand = cand && (S.lvl == 1 || (key >> (sh + 8)) == S.pre);
-                    digit = static_cast<int>((key >> sh) & 255u);
-                  }
-                  if (cand) {
-                    atomicAdd(hc + digit, 1u);
-                    atomicAdd(hm + digit, ex2((z - Mr) * k));
-                  }
+                if (z >= zlo && z < zhi) {
+                  const int digit = S.lvl == 0 ? vbin(z, Mr, k)
+                                               : static_cast<int>((okey<BF16>(z) >> sh) & 255u);
+                  atomicAdd(hc + digit, 1u);
+                  atomicAdd(hm + digit, ex2((z - Mr) * k));
                 }
               }
             }
