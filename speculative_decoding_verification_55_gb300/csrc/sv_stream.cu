@@ -3,9 +3,9 @@
 //
 // Work split. A position (b, i) of the batch is one target row (plus the draft row for a drafted
 // position) of V logits. Each cluster of C CTAs owns every nclusters-th position slot; CTA r of the
-// cluster owns the r-th contiguous chunk of every row it touches. Four CTAs share an SM, so one
-// CTA's exchanges and barriers overlap the others' arithmetic. A CTA is 4 consumer warps and one
-// producer warp.
+// cluster owns the r-th contiguous chunk of every row it touches. Four or five CTAs share an SM, so
+// one CTA's exchanges and barriers overlap the others' arithmetic. A CTA is 4 consumer warps and
+// one producer warp.
 //
 // Producer warp (one thread). Walks the cluster's positions and streams this CTA's chunks through a
 // ring of kNumSlots x kSlotBytes shared-memory slots with cp.async.bulk (the TMA engine), one full/empty
@@ -49,16 +49,25 @@
 namespace sv {
 namespace {
 
-// Four CTAs per SM, each 4 consumer warps + 1 producer warp with a 3 x 16 KB ring: four
+// Several CTAs per SM, each 4 consumer warps + 1 producer warp with a ring of 16 KB slots:
 // independent position streams per SM, so one CTA's exchange waits overlap another's arithmetic.
+// bf16 logits: five CTAs per SM with two slots each (V=256000: 1470 vs 1497 us with four CTAs and
+// three slots; V=128256: 72.8 vs 78.2 us). fp32 logits: four CTAs with three slots (five: 524 vs
+// 511 us at V=152064).
 #ifndef SV_STREAM_CONSUMER_WARPS
 #define SV_STREAM_CONSUMER_WARPS 4
 #endif
-#ifndef SV_STREAM_RING_SLOTS
-#define SV_STREAM_RING_SLOTS 3
+#ifndef SV_STREAM_RING_SLOTS_BF16
+#define SV_STREAM_RING_SLOTS_BF16 2
 #endif
-#ifndef SV_STREAM_CTAS_PER_SM
-#define SV_STREAM_CTAS_PER_SM 4
+#ifndef SV_STREAM_CTAS_PER_SM_BF16
+#define SV_STREAM_CTAS_PER_SM_BF16 5
+#endif
+#ifndef SV_STREAM_RING_SLOTS_F32
+#define SV_STREAM_RING_SLOTS_F32 3
+#endif
+#ifndef SV_STREAM_CTAS_PER_SM_F32
+#define SV_STREAM_CTAS_PER_SM_F32 4
 #endif
 constexpr int kCW = SV_STREAM_CONSUMER_WARPS;   // consumer warps
 constexpr int kCT = kCW * 32;                 // consumer threads
@@ -72,24 +81,31 @@ constexpr int kThreadsS = kCT + 32;           // plus the producer warp
 #endif
 constexpr int kSlotBytes = SV_STREAM_SLOT_BYTES;
 constexpr int kSlotUnits = kSlotBytes / 16;
-constexpr int kNumSlots = SV_STREAM_RING_SLOTS;
+template <bool BF16>
+constexpr int kSlotsOf = BF16 ? SV_STREAM_RING_SLOTS_BF16 : SV_STREAM_RING_SLOTS_F32;
+template <bool BF16>
+constexpr int kCtasPerSm = BF16 ? SV_STREAM_CTAS_PER_SM_BF16 : SV_STREAM_CTAS_PER_SM_F32;
+constexpr int kMaxSlots = SV_STREAM_RING_SLOTS_BF16 > SV_STREAM_RING_SLOTS_F32
+                              ? SV_STREAM_RING_SLOTS_BF16
+                              : SV_STREAM_RING_SLOTS_F32;
 static_assert(kSlotUnits % kCT == 0, "a ring slot splits evenly over the consumer threads");
 // A residual-pass slot holds kHalfUnits target vectors and the matching kHalfUnits draft vectors.
 constexpr int kHalfUnits = kSlotUnits / 2;
 static_assert(kHalfUnits % kCT == 0, "a residual slot splits evenly over the consumer threads");
-constexpr int kRingBytes = kSlotBytes * kNumSlots;
 constexpr int kGrp = SV_STREAM_GROUP;
 static_assert(kGrp == 1 || kGrp == 2 || kGrp == 4 || kGrp == 8, "groups of lanes for a shuffle sum");
 static_assert(kHalfUnits % kGrp == 0, "a vector group never straddles two ring slots");
 constexpr int kMaxGroups = (kStreamMaxUnits + kGrp - 1) / kGrp;
-constexpr int kDynBytes = kRingBytes + kMaxGroups * 4;   // ring, the draw's group weights
+// ring, then the draw's group weights
+template <bool BF16>
+constexpr int kDynBytesOf = kSlotBytes * kSlotsOf<BF16> + kMaxGroups * 4;
 constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
 
 enum : unsigned { kStatusTimeout = 1u };
 
 struct Shared {
-  uint64_t full[kNumSlots];
-  uint64_t empty[kNumSlots];
+  uint64_t full[kMaxSlots];
+  uint64_t empty[kMaxSlots];
   uint64_t xbar[2];                  // exchange: bytes pushed by every CTA complete it, by parity
   uint64_t xdone;                    // end-of-kernel arrivals
   float4 xrec[2][kMaxCluster];       // per rank: (m_p, s_p, m_q, s_q), or (argmax value, index)
@@ -307,9 +323,11 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
 constexpr uint32_t kXchBytes = 24;
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreadsS, SV_STREAM_CTAS_PER_SM) sv_stream_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Shared sm;
+  constexpr int kNumSlots = kSlotsOf<BF16>;
+  constexpr int kRingBytes = kSlotBytes * kNumSlots;
   constexpr size_t ES = BF16 ? 2 : 4;
   constexpr int E = BF16 ? 8 : 4;
 
@@ -915,10 +933,13 @@ const void* stream_fn(bool bf16) {
               : reinterpret_cast<const void*>(sv_stream_kernel<false>);
 }
 
-cudaError_t stream_attrs(const void* fn, int C) {
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBytes);
+int stream_dyn_bytes(bool bf16) { return bf16 ? kDynBytesOf<true> : kDynBytesOf<false>; }
+
+cudaError_t stream_attrs(const void* fn, int C, bool bf16) {
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       stream_dyn_bytes(bf16));
   if (e != cudaSuccess) return e;
-  // Two CTAs per SM need the largest shared-memory carveout.
+  // Several CTAs per SM need the largest shared-memory carveout.
   e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
@@ -926,11 +947,12 @@ cudaError_t stream_attrs(const void* fn, int C) {
   return e;
 }
 
-cudaLaunchConfig_t stream_config(int C, int nclusters, cudaStream_t stream, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t stream_config(int C, int nclusters, bool bf16, cudaStream_t stream,
+                                 cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * C), 1, 1);
   cfg.blockDim = dim3(kThreadsS, 1, 1);
-  cfg.dynamicSmemBytes = kDynBytes;
+  cfg.dynamicSmemBytes = stream_dyn_bytes(bf16);
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(C);
@@ -945,17 +967,17 @@ cudaLaunchConfig_t stream_config(int C, int nclusters, cudaStream_t stream, cuda
 
 cudaError_t stream_max_clusters(bool bf16, int C, int* n) {
   const void* fn = stream_fn(bf16);
-  const cudaError_t e = stream_attrs(fn, C);
+  const cudaError_t e = stream_attrs(fn, C, bf16);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = stream_config(C, 64, nullptr, attr);
+  cudaLaunchConfig_t cfg = stream_config(C, 64, bf16, nullptr, attr);
   return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
 }
 
 cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream) {
   const void* fn = stream_fn(bf16);
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = stream_config(P.C, P.nclusters, stream, attr);
+  cudaLaunchConfig_t cfg = stream_config(P.C, P.nclusters, bf16, stream, attr);
   void* args[] = {&P};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
