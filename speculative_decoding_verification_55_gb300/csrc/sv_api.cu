@@ -15,6 +15,16 @@ namespace {
 #ifndef SV_STREAM_CHUNK_BYTES
 #define SV_STREAM_CHUNK_BYTES 65536   // target bytes of one row chunk per CTA on the streaming path
 #endif
+// bf16 rows of a batch with many position slots per cluster: 128 KB chunks, half the CTAs per
+// position and so half the exchange participants (V=256000, B=1024: 1.28 vs 1.47 ms; one-hot
+// drafts 0.66 vs 0.89 ms). A small batch keeps SV_STREAM_CHUNK_BYTES to fill the GPU (B=64,
+// V=128256: 73 vs 76 us); fp32 rows too (B=256, V=152064: 513 vs 662 us).
+#ifndef SV_STREAM_CHUNK_BYTES_LARGE
+#define SV_STREAM_CHUNK_BYTES_LARGE 131072
+#endif
+#ifndef SV_STREAM_LARGE_MIN_SLOTS
+#define SV_STREAM_LARGE_MIN_SLOTS 16   // position slots per cluster that make a batch large
+#endif
 #ifndef SV_STREAM_MAX_CLUSTER
 #define SV_STREAM_MAX_CLUSTER 8
 #endif
@@ -49,15 +59,15 @@ bool element_plan(int V, int* vpt_index, int* C, int* per) {
   return false;
 }
 
-// Streaming path: CTAs per position, the power of two that brings a row chunk near
-// SV_STREAM_CHUNK_BYTES (at most SV_STREAM_MAX_CLUSTER), raised until a chunk fits the per-vector
-// sums buffer. 0 when even 16 CTAs leave chunks too large.
-int stream_cluster_size(long long row_bytes) {
+// Streaming path: CTAs per position, the power of two that brings a row chunk near chunk_bytes
+// (at most SV_STREAM_MAX_CLUSTER), raised until a chunk fits the group sums buffer. 0 when even 16
+// CTAs leave chunks too large.
+int stream_cluster_size(long long row_bytes, bool bf16,
+                        long long chunk_bytes = SV_STREAM_CHUNK_BYTES) {
   int C = 1;
-  while (C < SV_STREAM_MAX_CLUSTER && row_bytes > static_cast<long long>(C) * SV_STREAM_CHUNK_BYTES)
-    C *= 2;
+  while (C < SV_STREAM_MAX_CLUSTER && row_bytes > static_cast<long long>(C) * chunk_bytes) C *= 2;
   const long long units = row_bytes / 16;
-  while ((units + C - 1) / C > sv::kStreamMaxUnits) {
+  while ((units + C - 1) / C > sv::stream_max_units(bf16)) {
     if (C >= sv::kMaxCluster) return 0;
     C *= 2;
   }
@@ -99,6 +109,18 @@ int max_clusters(int dev, bool bf16, int C, int* n, bool filter = false) {
   }
   *n = slot;
   return SV_OK;
+}
+
+// CTAs per position on the streaming path: C (from SV_STREAM_CHUNK_BYTES), or for bf16 rows the
+// smaller C of SV_STREAM_CHUNK_BYTES_LARGE chunks when the batch holds at least
+// SV_STREAM_LARGE_MIN_SLOTS position slots per cluster of that size.
+int stream_plan_C(int dev, bool bf16, long long row_bytes, long long slots, int C) {
+  if (!bf16) return C;
+  const int Cl = stream_cluster_size(row_bytes, bf16, SV_STREAM_CHUNK_BYTES_LARGE);
+  if (Cl == 0 || Cl >= C) return C;
+  int mc = 0;
+  if (max_clusters(dev, bf16, Cl, &mc) != SV_OK) return C;
+  return slots >= static_cast<long long>(SV_STREAM_LARGE_MIN_SLOTS) * mc ? Cl : C;
 }
 
 }  // namespace
@@ -179,7 +201,8 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
     return (static_cast<size_t>(V) * es) % 16 != 0 ? SV_ERR_BAD_SHAPE : SV_ERR_MISALIGNED;
   int vpt_index = 0, eC = 1, eper = 1;
   if (!vec && !element_plan(V, &vpt_index, &eC, &eper)) return SV_ERR_BAD_SHAPE;
-  const int sC = vec ? stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es)) : 0;
+  const int sC =
+      vec ? stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es), bf16) : 0;
   if (vec && sC == 0) return SV_ERR_BAD_SHAPE;
 
   int dev = 0;
@@ -210,12 +233,12 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
 
   if (vec) {
     const int E = static_cast<int>(16 / es);
+    const long long slots = static_cast<long long>(B) * (G + 1);
     P.units = V / E;
-    P.C = sC;
+    P.C = stream_plan_C(dev, bf16, static_cast<long long>(V) * static_cast<long long>(es), slots, sC);
     P.per = (P.units + P.C - 1) / P.C;
     int maxc = 0;
     if (max_clusters(dev, bf16, P.C, &maxc) != SV_OK) return SV_ERR_CUDA;
-    const long long slots = static_cast<long long>(B) * (G + 1);
     P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
     if (sv::launch_stream(P, bf16, stream) != cudaSuccess) return SV_ERR_CUDA;
     return SV_OK;
@@ -266,7 +289,7 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
   // Tree rows run on the streaming kernel only (rows of 16-byte multiples, 16-byte aligned base).
   if ((static_cast<size_t>(V) * es) % 16 != 0) return SV_ERR_BAD_SHAPE;
   if (reinterpret_cast<uintptr_t>(target_logits) % 16 != 0) return SV_ERR_MISALIGNED;
-  const int sC = stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es));
+  const int sC = stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es), bf16);
   if (sC == 0) return SV_ERR_BAD_SHAPE;
   int dev = 0;
   const int dev_status = check_device(&dev);
@@ -290,12 +313,12 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
   P.G = G;
   P.V = V;
   const int E = static_cast<int>(16 / es);
+  const long long slots = static_cast<long long>(B) * N;
   P.units = V / E;
-  P.C = sC;
+  P.C = stream_plan_C(dev, bf16, static_cast<long long>(V) * static_cast<long long>(es), slots, sC);
   P.per = (P.units + P.C - 1) / P.C;
   int maxc = 0;
   if (max_clusters(dev, bf16, P.C, &maxc) != SV_OK) return SV_ERR_CUDA;
-  const long long slots = static_cast<long long>(B) * N;
   P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
   if (sv::launch_stream(P, bf16, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
     return SV_ERR_CUDA;

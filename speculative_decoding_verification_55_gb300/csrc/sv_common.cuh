@@ -22,9 +22,18 @@ namespace sv {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kMaxCluster = 16;
-// Largest chunk (in 16-byte vectors) one CTA of the streaming kernel owns per row: its per-vector
-// residual sums must fit in shared memory beside the copy ring.
-constexpr int kStreamMaxUnits = 4864;
+// Largest chunk (in 16-byte vectors) one CTA of the streaming kernel owns per row: its group
+// sums of the residual weights must fit in shared memory beside the copy ring (bf16: a two-slot
+// ring, 128 KB chunks; fp32: a three-slot ring).
+#ifndef SV_STREAM_MAX_UNITS_BF16
+#define SV_STREAM_MAX_UNITS_BF16 8192
+#endif
+#ifndef SV_STREAM_MAX_UNITS_F32
+#define SV_STREAM_MAX_UNITS_F32 4864
+#endif
+constexpr int stream_max_units(bool bf16) {
+  return bf16 ? SV_STREAM_MAX_UNITS_BF16 : SV_STREAM_MAX_UNITS_F32;
+}
 
 enum : int { kVerify = 0, kBonus = 1, kArgmax = 2, kOneHot = 3 };
 enum : int { kFlagAccept = 1, kFlagBad = 2, kFlagDone = 4 };

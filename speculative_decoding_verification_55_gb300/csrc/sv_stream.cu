@@ -95,10 +95,11 @@ static_assert(kHalfUnits % kCT == 0, "a residual slot splits evenly over the con
 constexpr int kGrp = SV_STREAM_GROUP;
 static_assert(kGrp == 1 || kGrp == 2 || kGrp == 4 || kGrp == 8, "groups of lanes for a shuffle sum");
 static_assert(kHalfUnits % kGrp == 0, "a vector group never straddles two ring slots");
-constexpr int kMaxGroups = (kStreamMaxUnits + kGrp - 1) / kGrp;
+template <bool BF16>
+constexpr int kMaxGroupsOf = (stream_max_units(BF16) + kGrp - 1) / kGrp;
 // ring, then the draw's group weights
 template <bool BF16>
-constexpr int kDynBytesOf = kSlotBytes * kSlotsOf<BF16> + kMaxGroups * 4;
+constexpr int kDynBytesOf = kSlotBytes * kSlotsOf<BF16> + kMaxGroupsOf<BF16> * 4;
 constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
 
 enum : unsigned { kStatusTimeout = 1u };
