@@ -269,3 +269,25 @@ def test_gpu_tree_workspace_left_zeroed(sv):
     ws = sv.workspace_for(6, 8, 2048, sv.SV_DTYPE_F32, torch.device("cuda"))
     assert int(ws.count_nonzero()) == 0
     assert sv.spec_verify_workspace_status(ws, 6, 8) == 0
+
+
+@pytest.mark.gpu
+def test_gpu_tree_full_size_batch(sv):
+    """The benchmark's tree batch (B=256 Medusa trees of 31 nodes, V=128256 bf16): enough position
+    slots that the streaming path takes its large-chunk clusters. A seeded sample of rows against
+    the oracle."""
+    import importlib.util
+    from pathlib import Path
+    spec = importlib.util.spec_from_file_location(
+        "bench_for_tree", Path(__file__).resolve().parent.parent / "bench.py")
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    zt, tok, par = bench.tree_inputs(bench.TREE_B, 7, "torch")
+    out = sv.verify_tree(zt, tok, par, None)
+    torch.cuda.synchronize()
+    gpu = [o.cpu().numpy() for o in out]
+    rows = np.sort(np.random.default_rng(11).choice(bench.TREE_B, 16, replace=False))
+    idx = torch.from_numpy(rows).cuda()
+    r = oracle_tree_greedy(zt[idx].float().cpu().numpy(), tok[idx].cpu().numpy(),
+                           par[idx].cpu().numpy())
+    check_tree(r, [g[rows] for g in gpu])
