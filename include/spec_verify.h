@@ -191,6 +191,8 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
  * top_k  [B] int32  per-row k; <= 0 or >= V turns top-k off. NULL: off for every row.
  * top_p  [B] fp32   per-row nucleus mass; >= 1 turns top-p off; a sampled row with top_p NaN or
  *                   <= 0 is a row error (outputs -1 / 0). NULL: off for every row.
+ * The call enqueues two kernels on `cuda_stream`: the streaming kernel of spec_verify_ex for the
+ * rows whose filters are off and the greedy rows, then the filter kernel for the other rows.
  * Everything else (arguments, layout, ownership, workspace, errors) as in spec_verify_ex. Only rows
  * of 16-byte multiples are supported (else SV_ERR_BAD_SHAPE), with 16-byte aligned logit bases
  * (else SV_ERR_MISALIGNED), and V at most 16 * 65536 bytes of logits per row (bf16 V <= 524288,

@@ -400,6 +400,23 @@ int spec_verify_filtered(const void* target_logits, const void* draft_logits,
   if (max_clusters(dev, bf16, C, &maxc, true) != SV_OK) return SV_ERR_CUDA;
   const long long slots = static_cast<long long>(B) * (G + 1);
   P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
+  // Rows whose filters keep every token, and greedy rows, run on the streaming kernel (the same
+  // outputs as spec_verify_ex, without the filter kernel's selections); the filter kernel takes
+  // the others. Both write disjoint rows of the same outputs and workspace.
+  const long long row_bytes = static_cast<long long>(V) * static_cast<long long>(es);
+  const int sC = stream_cluster_size(row_bytes, bf16);
+  if (sC > 0) {
+    sv::Params S = P;
+    S.C = stream_plan_C(dev, bf16, row_bytes, slots, sC);
+    S.per = (S.units + S.C - 1) / S.C;
+    int smax = 0;
+    if (max_clusters(dev, bf16, S.C, &smax) != SV_OK) return SV_ERR_CUDA;
+    S.nclusters = static_cast<int>(slots < smax ? slots : smax);
+    S.split = 1;
+    P.split = 1;
+    if (sv::launch_stream(S, bf16, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
   if (sv::launch_filter(P, bf16, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;

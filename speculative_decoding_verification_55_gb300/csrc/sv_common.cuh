@@ -70,6 +70,9 @@ struct Params {
   // Filtered verification (filter kernel): per-row top-k and top-p, applied to p and q alike.
   const int32_t* top_k;      // [B] or null (0 or >= V: off)
   const float* top_p;        // [B] or null (>= 1: off)
+  // Filtered verification in two launches (split != 0): the streaming kernel takes the rows that
+  // row_unfiltered picks, the filter kernel the others.
+  int split;
 };
 
 constexpr int kMaxTreeNodes = 65;    // N <= SV_MAX_GAMMA + 1
@@ -497,6 +500,16 @@ __device__ __forceinline__ float p_vec_sum(const uint4& t, float k, float cb) {
 // ------------------------------------------------------------------------------------------------
 // Row scalars and row errors
 // ------------------------------------------------------------------------------------------------
+
+// A row whose filters keep every token (top_k off or >= V, top_p >= 1), or a greedy row (the
+// filters keep its argmax): the same outputs as without filters. A NaN or non-positive top_p is
+// not unfiltered (the filter kernel reports it as a row error).
+__device__ __forceinline__ bool row_unfiltered(const Params& P, int b) {
+  if (__ldg(P.temperature + b) == 0.0f) return true;
+  const int k = P.top_k ? __ldg(P.top_k + b) : 0;
+  const float pp = P.top_p ? __ldg(P.top_p + b) : 1.0f;
+  return (k <= 0 || k >= P.V) && pp >= 1.0f;
+}
 
 // Writes the all-error outputs of row b (one full warp).
 __device__ __forceinline__ void write_row_error(const Params& P, int b, int lane) {

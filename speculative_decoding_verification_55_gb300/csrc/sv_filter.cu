@@ -120,6 +120,10 @@ __device__ __forceinline__ FPos fclassify(const Params& P, int s) {
   p.t_ok = p.greedy || (p.T >= FLT_MIN && p.T <= FLT_MAX);   // NaN fails both
   p.load = p.len_ok && p.t_ok && p.i <= p.gb;
   p.two = p.load && !p.greedy && p.i < p.gb;
+  if (P.split && row_unfiltered(P, p.b)) {    // the streaming kernel's row: no work, no error here
+    p.len_ok = p.t_ok = true;
+    p.load = p.two = false;
+  }
   return p;
 }
 

@@ -26,7 +26,8 @@
 //            (an inclusive scan over ranks = the chunk-level CDF of p), the accept test
 //            u < min(1, p(x)/q(x)), the chunk that holds a bonus-draw threshold.
 //   pass 2   (drafted positions) the chunk again, copied from L2 where pass 1 left it through
-//            the same ring (each slot half target vectors, half the matching draft vectors):
+//            the same ring, last block first (each slot half target vectors, half the matching
+//            draft vectors):
 //            residual weights max(0, p - q), p and q normalised inside the exponent; one sum per
 //            group of kGrp 16-byte vectors is kept in shared memory for the draw. alpha = 1 - W
 //            with W the residual mass: sum min(p, q) + sum max(0, p - q) = sum p = 1 ([R] Why the
@@ -171,6 +172,10 @@ __device__ __forceinline__ Pos classify(const Params& P, int s) {
   p.load = p.len_ok && p.t_ok && p.i <= p.gb;
   p.two = p.load && !p.greedy && p.i < p.gb && !P.onehot;
   p.oh = p.load && !p.greedy && p.i < p.gb && P.onehot;
+  if (P.split && !row_unfiltered(P, p.b)) {   // the filter kernel's row: no work, no error here
+    p.len_ok = p.t_ok = true;
+    p.load = p.two = p.oh = false;
+  }
   return p;
 }
 
@@ -389,8 +394,9 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       }
       if (!p.two || !ok) continue;
       // Residual pass of a drafted position: the same chunk again, now from L2, each slot holding
-      // kHalfUnits target vectors and the matching draft vectors. These copies depend on nothing
-      // the exchange produces, so they land while the consumers wait for it.
+      // kHalfUnits target vectors and the matching draft vectors, last block first (the most
+      // recently streamed lines are the likeliest still in L2). These copies depend on nothing the
+      // exchange produces, so they land while the consumers wait for it.
       const char* gt = static_cast<const char*>(P.zt) + ((size_t)p.b * G1 + p.i) * Vs * ES + (size_t)u0 * 16;
       const char* gd = static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES + (size_t)u0 * 16;
       for (int ks = 0; ks < nsl2; ++ks, ++tc) {
@@ -399,8 +405,9 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
           ok = false;
           break;
         }
-        const uint32_t bytes = static_cast<uint32_t>(min(kHalfUnits, cu - ks * kHalfUnits)) * 16;
-        const size_t off = static_cast<size_t>(ks) * kHalfUnits * 16;
+        const int blk = nsl2 - 1 - ks;
+        const uint32_t bytes = static_cast<uint32_t>(min(kHalfUnits, cu - blk * kHalfUnits)) * 16;
+        const size_t off = static_cast<size_t>(blk) * kHalfUnits * 16;
         mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), 2 * bytes);
         bulk_g2s(ring_addr + slot * kSlotBytes, gt + off, bytes, smem_addr(&sm.full[slot]), once);
         bulk_g2s(ring_addr + slot * kSlotBytes + kSlotBytes / 2, gd + off, bytes,
@@ -871,7 +878,8 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
         // Warp-uniform, so that a wait given up by one lane cannot split a group's shuffle.
         if (!__all_sync(kFull, mbar_wait(smem_addr(&sm.full[slot]), par))) tmo = true;
-        const int nu = min(kHalfUnits, cu - ks * kHalfUnits);
+        const int blk = nsl2 - 1 - ks;               // the producer's order: last block first
+        const int nu = min(kHalfUnits, cu - blk * kHalfUnits);
         const uint4* st4 = ringv + slot * kSlotUnits;
         const uint4* sd4 = st4 + kHalfUnits;
         if (!cbad && !tmo) {
@@ -883,7 +891,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
             const float sv = uu < nu ? resid_vec_sum<BF16>(st4[uu], sd4[uu], k2, c2) : 0.0f;
             W += sv;
             const float g = group_sum(sv);
-            if ((ctid & (kGrp - 1)) == 0 && uu < nu) usum[(ks * kHalfUnits + uu) / kGrp] = g;
+            if ((ctid & (kGrp - 1)) == 0 && uu < nu) usum[(blk * kHalfUnits + uu) / kGrp] = g;
           }
         }
         __syncwarp();
