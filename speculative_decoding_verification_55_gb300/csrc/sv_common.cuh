@@ -31,8 +31,10 @@ constexpr int kMaxCluster = 16;
 #ifndef SV_STREAM_MAX_UNITS_F32
 #define SV_STREAM_MAX_UNITS_F32 4864
 #endif
-constexpr int stream_max_units(bool bf16) {
-  return bf16 ? SV_STREAM_MAX_UNITS_BF16 : SV_STREAM_MAX_UNITS_F32;
+// wide: the draw groups of bf16 one-hot launches, twice as long (twice the chunk, same table).
+constexpr int stream_max_units(bool bf16, bool wide = false) {
+  return bf16 ? (wide ? 2 * SV_STREAM_MAX_UNITS_BF16 : SV_STREAM_MAX_UNITS_BF16)
+              : SV_STREAM_MAX_UNITS_F32;
 }
 
 enum : int { kVerify = 0, kBonus = 1, kArgmax = 2, kOneHot = 3 };
@@ -714,7 +716,7 @@ cudaError_t launch_element(const Params& P, bool bf16, int vpt_index, cudaStream
 // Streaming path (16-byte aligned rows): persistent clusters fed by bulk copies.
 cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream);
 // Clusters of `C` CTAs of the streaming kernel that fit on the current device at once.
-cudaError_t stream_max_clusters(bool bf16, int C, int* n);
+cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n);
 // Filtered verification (16-byte aligned rows of at most 16 chunks of filter_max_row_units()
 // vectors): persistent clusters, one position per cluster at a time.
 cudaError_t launch_filter(Params P, bool bf16, cudaStream_t stream);

@@ -29,7 +29,8 @@
 //            the same ring, last block first (each slot half target vectors, half the matching
 //            draft vectors):
 //            residual weights max(0, p - q), p and q normalised inside the exponent; one sum per
-//            group of kGrp 16-byte vectors is kept in shared memory for the draw. alpha = 1 - W
+//            group of kGrp 16-byte vectors (4, or 8 for bf16 one-hot launches) is kept in shared
+//            memory for the draw. alpha = 1 - W
 //            with W the residual mass: sum min(p, q) + sum max(0, p - q) = sum p = 1 ([R] Why the
 //            output is exactly the target's).
 //   next     the residual chunk totals (inclusive scan over ranks) arrive with the next exchange.
@@ -93,14 +94,19 @@ static_assert(kSlotUnits % kCT == 0, "a ring slot splits evenly over the consume
 // A residual-pass slot holds kHalfUnits target vectors and the matching kHalfUnits draft vectors.
 constexpr int kHalfUnits = kSlotUnits / 2;
 static_assert(kHalfUnits % kCT == 0, "a residual slot splits evenly over the consumer threads");
-constexpr int kGrp = SV_STREAM_GROUP;
-static_assert(kGrp == 1 || kGrp == 2 || kGrp == 4 || kGrp == 8, "groups of lanes for a shuffle sum");
-static_assert(kHalfUnits % kGrp == 0, "a vector group never straddles two ring slots");
-template <bool BF16>
-constexpr int kMaxGroupsOf = (stream_max_units(BF16) + kGrp - 1) / kGrp;
+// Draw groups: kGrpNarrow vectors per group, or kGrpWide for bf16 one-hot launches, which take
+// chunks twice as long (the group table keeps its size).
+constexpr int kGrpNarrow = SV_STREAM_GROUP;
+constexpr int kGrpWide = 8;
+static_assert(kGrpNarrow == 1 || kGrpNarrow == 2 || kGrpNarrow == 4 || kGrpNarrow == 8,
+              "groups of lanes for a shuffle sum");
+static_assert(kHalfUnits % kGrpWide == 0 && kHalfUnits % kGrpNarrow == 0,
+              "a vector group never straddles two ring slots");
+template <bool BF16, int G>
+constexpr int kMaxGroupsOf = (stream_max_units(BF16, G == kGrpWide) + G - 1) / G;
 // ring, then the draw's group weights
-template <bool BF16>
-constexpr int kDynBytesOf = kSlotBytes * kSlotsOf<BF16> + kMaxGroupsOf<BF16> * 4;
+template <bool BF16, int G>
+constexpr int kDynBytesOf = kSlotBytes * kSlotsOf<BF16> + kMaxGroupsOf<BF16, G> * 4;
 constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
 
 enum : unsigned { kStatusTimeout = 1u };
@@ -200,11 +206,12 @@ __device__ __forceinline__ uint4 mask_elem(uint4 v, int e) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Sum over the kGrp consecutive lanes of a group (vectors u, u+1, ... of a chunk sit in
-// consecutive lanes); every lane of the group gets the total.
+// Sum over the G consecutive lanes of a group (vectors u, u+1, ... of a chunk sit in consecutive
+// lanes); every lane of the group gets the total.
+template <int G>
 __device__ __forceinline__ float group_sum(float v) {
 #pragma unroll
-  for (int o = 1; o < kGrp; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
+  for (int o = 1; o < G; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
   return v;
 }
 
@@ -214,7 +221,7 @@ __device__ __forceinline__ float group_sum(float v) {
 // group sums, then one reload of the crossing group. Returns the token in warp `finisher` (all its
 // lanes); other warps return -1. All consumer threads call it. Token `skip_tok` (if >= 0) has weight 0
 // (the usum entries already leave it out).
-template <bool BF16>
+template <bool BF16, int kGrp>
 __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, const char* rowt,
                           const char* rowd, bool resid, float k, float ct, float cd, float cb,
                           Shared& sm, int ctid, int& finisher, int skip_tok = -1) {
@@ -328,7 +335,7 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
 // Bytes every CTA pushes into every CTA of its cluster per exchange: one float4 record and one uint2.
 constexpr uint32_t kXchBytes = 24;
 
-template <bool BF16>
+template <bool BF16, int kGrp>
 __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Shared sm;
@@ -449,7 +456,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float g = group_sum(p_vec_sum<BF16>(t[j], kk, cbv));
+        const float g = group_sum<kGrp>(p_vec_sum<BF16>(t[j], kk, cbv));
         if ((ctid & (kGrp - 1)) == 0) usum[(base + ctid + j * kCT) / kGrp] = g;
       }
     }
@@ -461,7 +468,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         if (uu == xu) t = mask_elem<BF16>(t, excl - (u0 + xu) * E);
         sv = p_vec_sum<BF16>(t, kk, cbv);
       }
-      const float g = group_sum(sv);
+      const float g = group_sum<kGrp>(sv);
       if ((ctid & (kGrp - 1)) == 0 && uu < cu) usum[uu / kGrp] = g;
     }
   };
@@ -655,8 +662,8 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       named_bar_sync(kConsumerBar, kCT);
     }
     int finisher = 0;
-    const int tok = chunk_draw<BF16>(usum, cu, u0, tl, prt, prd, resid, pkk, pct, pcd, pcb, sm, ctid,
-                                     finisher);
+    const int tok = chunk_draw<BF16, kGrp>(usum, cu, u0, tl, prt, prd, resid, pkk, pct, pcd, pcb, sm,
+                                           ctid, finisher);
     if (cw == finisher) finish_position(P, pb, pi, pgb, tok, tok < 0 ? kFlagBad : 0, alpha, ppx, pqx,
                                         lane);
   };
@@ -833,8 +840,8 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         fill_p_sums(rowt, kk, cb, x);
         named_bar_sync(kConsumerBar, kCT);
         int finisher = 0;
-        const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm, ctid,
-                                         finisher, x);
+        const int tok = chunk_draw<BF16, kGrp>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm,
+                                               ctid, finisher, x);
         if (cw == finisher)
           finish_position(P, p.b, p.i, p.gb, tok, tok < 0 ? kFlagBad : 0, apx, apx, 1.0f, lane);
       }
@@ -860,8 +867,8 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         fill_p_sums(rowt, kk, cb, -1);
         named_bar_sync(kConsumerBar, kCT);
         int finisher = 0;
-        const int tok = chunk_draw<BF16>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm, ctid,
-                                         finisher);
+        const int tok = chunk_draw<BF16, kGrp>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm,
+                                               ctid, finisher);
         if (cw == finisher)
           finish_position(P, p.b, p.i, p.gb, tok, (tok < 0 ? kFlagBad : 0) | kFlagAccept, 0.0f, 0.0f,
                           0.0f, lane);
@@ -890,7 +897,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
             const int uu = ctid + j * kCT;
             const float sv = uu < nu ? resid_vec_sum<BF16>(st4[uu], sd4[uu], k2, c2) : 0.0f;
             W += sv;
-            const float g = group_sum(sv);
+            const float g = group_sum<kGrp>(sv);
             if ((ctid & (kGrp - 1)) == 0 && uu < nu) usum[(blk * kHalfUnits + uu) / kGrp] = g;
           }
         }
@@ -937,16 +944,23 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
   }
 }
 
-const void* stream_fn(bool bf16) {
-  return bf16 ? reinterpret_cast<const void*>(sv_stream_kernel<true>)
-              : reinterpret_cast<const void*>(sv_stream_kernel<false>);
+// bf16 one-hot launches take the wide draw groups; the rest the narrow ones.
+const void* stream_fn(bool bf16, bool wide) {
+  if (bf16) {
+    return wide ? reinterpret_cast<const void*>(sv_stream_kernel<true, kGrpWide>)
+                : reinterpret_cast<const void*>(sv_stream_kernel<true, kGrpNarrow>);
+  }
+  return reinterpret_cast<const void*>(sv_stream_kernel<false, kGrpNarrow>);
 }
 
-int stream_dyn_bytes(bool bf16) { return bf16 ? kDynBytesOf<true> : kDynBytesOf<false>; }
+int stream_dyn_bytes(bool bf16, bool wide) {
+  if (bf16) return wide ? kDynBytesOf<true, kGrpWide> : kDynBytesOf<true, kGrpNarrow>;
+  return kDynBytesOf<false, kGrpNarrow>;
+}
 
-cudaError_t stream_attrs(const void* fn, int C, bool bf16) {
+cudaError_t stream_attrs(const void* fn, int C, bool bf16, bool wide) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       stream_dyn_bytes(bf16));
+                                       stream_dyn_bytes(bf16, wide));
   if (e != cudaSuccess) return e;
   // Several CTAs per SM need the largest shared-memory carveout.
   e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -956,12 +970,12 @@ cudaError_t stream_attrs(const void* fn, int C, bool bf16) {
   return e;
 }
 
-cudaLaunchConfig_t stream_config(int C, int nclusters, bool bf16, cudaStream_t stream,
+cudaLaunchConfig_t stream_config(int C, int nclusters, bool bf16, bool wide, cudaStream_t stream,
                                  cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * C), 1, 1);
   cfg.blockDim = dim3(kThreadsS, 1, 1);
-  cfg.dynamicSmemBytes = stream_dyn_bytes(bf16);
+  cfg.dynamicSmemBytes = stream_dyn_bytes(bf16, wide);
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(C);
@@ -974,19 +988,21 @@ cudaLaunchConfig_t stream_config(int C, int nclusters, bool bf16, cudaStream_t s
 
 }  // namespace
 
-cudaError_t stream_max_clusters(bool bf16, int C, int* n) {
-  const void* fn = stream_fn(bf16);
-  const cudaError_t e = stream_attrs(fn, C, bf16);
+cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n) {
+  wide = wide && bf16;
+  const void* fn = stream_fn(bf16, wide);
+  const cudaError_t e = stream_attrs(fn, C, bf16, wide);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = stream_config(C, 64, bf16, nullptr, attr);
+  cudaLaunchConfig_t cfg = stream_config(C, 64, bf16, wide, nullptr, attr);
   return cudaOccupancyMaxActiveClusters(n, fn, &cfg);
 }
 
 cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream) {
-  const void* fn = stream_fn(bf16);
+  const bool wide = bf16 && P.onehot;
+  const void* fn = stream_fn(bf16, wide);
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = stream_config(P.C, P.nclusters, bf16, stream, attr);
+  cudaLaunchConfig_t cfg = stream_config(P.C, P.nclusters, bf16, wide, stream, attr);
   void* args[] = {&P};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
