@@ -18,8 +18,11 @@
 //       refine the chosen bin on 8-bit digits of the logit's order key (2 levels for bf16, 4 for
 //       fp32), and a selection stops early once the boundary bin is decided whole. Every level is
 //       a count and mass histogram per CTA, read across the cluster in rank order, so every CTA
-//       sums the same numbers in the same order and takes the same decision.
-//   V   the filtered p~ (and q~): the accept test u < min(1, p~(x)/q~(x)), then the chunk totals of
+//       sums the same numbers in the same order and takes the same decision. A level's candidates
+//       are one interval of floats (kept_threshold finds its ends), so a logit outside it costs
+//       two compares.
+//   V   the filtered p~ (and q~), a logit kept when z >= the row's smallest kept float: the
+//       accept test u < min(1, p~(x)/q~(x)), then the chunk totals of
 //       max(0, p~ - q~) and of p~ in one exchange: alpha = 1 - sum max(0, p~ - q~), and the chunk
 //       holding the draw's threshold (the residual draw, its fallback to p~, or the bonus draw).
 //   D   that CTA scans its chunk in index order (block-wide prefix sum over per-thread runs) and
@@ -28,7 +31,10 @@
 //       the max gives the bin of the k-th largest logit, one pass writes every logit of that bin
 //       or above (a superset of the top-k set, typically k plus a few) into a per-CTA list, and
 //       when the lists fit, rank 0 gathers them in index order and runs K, P, V and D on them
-//       alone while the other CTAs move on. Same levels and decisions as the chunk-wide passes.
+//       alone while the other CTAs move on (and every CTA starts the next position's copies).
+//       Same levels and decisions as the chunk-wide passes.
+// With Params::split the kernel takes only the rows that row_unfiltered leaves out; the streaming
+// kernel verifies the others in the same call.
 // Control flow depends on cluster-wide data only, so every CTA passes the same cluster barriers.
 // The bulk-copy wait is bounded; a CTA whose wait gives up reports it in the next exchange, the
 // position is marked bad, the status word is set and the cluster stops.
