@@ -210,28 +210,46 @@ __device__ void level_interval(const FSel& S, float M, float k, int lane, float&
   else zhi = S.D0 == 255 ? INFINITY : kept_threshold<BF16>(M, k, S.D0 + 1, 0u, lane);
 }
 
-__device__ __forceinline__ float block_sum(float v, FShared& sm, int slot) {
+// Block-wide max (NaN-propagating) and sum of the two rows of a position at once, in warp order
+// (one pair of barriers each).
+__device__ __forceinline__ void block_max2_nan(float& a, float& b, FShared& sm) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  v = warp_sum_lane0(v);
-  if (lane == 0) sm.redf[w][slot] = v;
+  a = warp_max_nan(a);
+  b = warp_max_nan(b);
+  if (lane == 0) {
+    sm.redf[w][0] = a;
+    sm.redf[w][1] = b;
+  }
   __syncthreads();
-  float t = 0.0f;
+  float ta = -INFINITY, tb = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < kFW; ++j) t += sm.redf[j][slot];
+  for (int j = 0; j < kFW; ++j) {
+    ta = max_nan(ta, sm.redf[j][0]);
+    tb = max_nan(tb, sm.redf[j][1]);
+  }
   __syncthreads();
-  return t;
+  a = ta;
+  b = tb;
 }
 
-__device__ __forceinline__ float block_max_nan(float v, FShared& sm, int slot) {
+__device__ __forceinline__ void block_sum2(float& a, float& b, FShared& sm) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  v = warp_max_nan(v);
-  if (lane == 0) sm.redf[w][slot] = v;
+  a = warp_sum_lane0(a);
+  b = warp_sum_lane0(b);
+  if (lane == 0) {
+    sm.redf[w][2] = a;
+    sm.redf[w][3] = b;
+  }
   __syncthreads();
-  float t = -INFINITY;
+  float ta = 0.0f, tb = 0.0f;
 #pragma unroll
-  for (int j = 0; j < kFW; ++j) t = max_nan(t, sm.redf[j][slot]);
+  for (int j = 0; j < kFW; ++j) {
+    ta += sm.redf[j][2];
+    tb += sm.redf[j][3];
+  }
   __syncthreads();
-  return t;
+  a = ta;
+  b = tb;
 }
 
 __device__ __forceinline__ unsigned warp_incl_scan_u(unsigned v, int lane) {
@@ -635,23 +653,29 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
     const bool pon = ok && topp < 1.0f;
     const bool filt = kon || pon;
     float lm[2] = {-INFINITY, -INFINITY}, ls[2] = {0.0f, 0.0f};
+    if (landed) {
+      for (int u = tid; u < cu; u += kFT) lm[0] = max_nan(lm[0], vec_max<BF16>(dt[u]));
+      if (nrows > 1)
+        for (int u = tid; u < cu; u += kFT) lm[1] = max_nan(lm[1], vec_max<BF16>(dd[u]));
+    }
+    block_max2_nan(lm[0], lm[1], sm);
     int lbad = 0;
-    for (int r = 0; r < nrows; ++r) {
-      const uint4* src = r == 0 ? dt : dd;
-      float m = -INFINITY;
-      if (landed)
-        for (int u = tid; u < cu; u += kFT) m = max_nan(m, vec_max<BF16>(src[u]));
-      m = block_max_nan(m, sm, r);
-      lbad |= (m != m) || m == INFINITY;
-      float sum = 0.0f;
-      if (!filt && landed && m > -INFINITY && m < INFINITY)
-        for (int u = tid; u < cu; u += kFT) {
-          const uint4 v = src[u];
 #pragma unroll
-          for (int e = 0; e < E; ++e) sum += ex2((vec_get<BF16>(v, e) - m) * k);
-        }
-      lm[r] = m;
-      ls[r] = filt ? 0.0f : block_sum(sum, sm, 2 + r);
+    for (int r = 0; r < 2; ++r)
+      if (r < nrows) lbad |= (lm[r] != lm[r]) || lm[r] == INFINITY;
+    if (!filt) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint4* src = r == 0 ? dt : dd;
+        const float m = lm[r];
+        if (r < nrows && landed && m > -INFINITY && m < INFINITY)
+          for (int u = tid; u < cu; u += kFT) {
+            const uint4 v = src[u];
+#pragma unroll
+            for (int e = 0; e < E; ++e) ls[r] += ex2((vec_get<BF16>(v, e) - m) * k);
+          }
+      }
+      block_sum2(ls[0], ls[1], sm);
     }
     if (tid == 0) {
       const uint32_t par = ex & 1;
@@ -879,6 +903,18 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
             }
           }
           if (rank != 0) continue;
+          // warp 0's global reads for the accept test and the draw, issued first so that their
+          // latency passes under the gathering and the selections
+          float e_zt = 0.0f, e_zd = 0.0f, e_uacc = 0.0f, e_udraw = 0.0f;
+          if (warp == 0) {
+            const float* ur = P.uniforms + (size_t)p.b * (G + 2);
+            if (p.two) {
+              e_zt = load_logit<BF16>(rowt, x);
+              e_zd = load_logit<BF16>(rowd, x);
+              e_uacc = __ldg(ur + p.i);
+            }
+            e_udraw = p.two ? __ldg(ur + G) : __ldg(ur + G + 1);
+          }
           // gather: CTA q's target entries go to loff[q] + their rank by index (chunks are in index
           // order by rank, so the list is in index order); draft entries in any order
           for (int j = tid; j < N0; j += kFT) {
@@ -939,10 +975,10 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
             };
             float px = 0.0f, qx = 0.0f, acc = 1.0f;
             if (p.two) {
-              px = wt_l(load_logit<BF16>(rowt, x));
-              qx = wd_l(load_logit<BF16>(rowd, x));
+              px = wt_l(e_zt);
+              qx = wd_l(e_zd);
               const float ratio = (qx > 0.0f) ? fminf(1.0f, px / qx) : 1.0f;
-              acc = __ldg(P.uniforms + (size_t)p.b * (G + 2) + p.i) < ratio ? 1.0f : 0.0f;
+              acc = e_uacc < ratio ? 1.0f : 0.0f;
             }
             const int run = (N0 + 31) / 32;
             const int e0 = min(lane * run, N0), e1 = min(e0 + run, N0);
@@ -966,8 +1002,7 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
             } else {
               // the residual (rejection), p~ when the residual has no mass, or the bonus draw
               const bool resid = p.two && Wt > 0.0f;
-              const float* ur = P.uniforms + (size_t)p.b * (G + 2);
-              const float uu = p.two ? __ldg(ur + G) : __ldg(ur + G + 1);
+              const float uu = e_udraw;
               const float t = uu * (resid ? Wt : Pt);
               const float ts = resid ? sw : sp, incl = resid ? iw : ip;
               float excl = __shfl_up_sync(kFull, incl, 1);
@@ -1179,8 +1214,7 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
         }
       }
     }
-    wsum = block_sum(wsum, sm, 0);
-    psum = block_sum(psum, sm, 1);
+    block_sum2(wsum, psum, sm);
     if (tid == 0) {
       const uint32_t par = ex & 1;
       sm.xrec[par][0] = wsum;
