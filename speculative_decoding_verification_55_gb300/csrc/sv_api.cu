@@ -133,6 +133,18 @@ int stream_plan_C(int dev, bool bf16, long long row_bytes, long long slots, int 
   return slots >= static_cast<long long>(SV_STREAM_LARGE_MIN_SLOTS) * mc ? Cl : C;
 }
 
+// Greedy tree nodes draw nothing, so the draw-group table does not bound their chunks: a batch
+// with at least 8 node slots per cluster takes chunks of up to SV_STREAM_CHUNK_BYTES_ONEHOT
+// (one CTA per node row at V=128256 bf16); otherwise the plan of stream_plan_C.
+int tree_plan_C(int dev, bool bf16, long long row_bytes, long long slots, int C) {
+  const int Ct = stream_cluster_size(row_bytes, bf16, SV_STREAM_CHUNK_BYTES_ONEHOT, true);
+  if (bf16 && Ct > 0 && Ct < C) {
+    int mc = 0;
+    if (max_clusters(dev, bf16, Ct, &mc) == SV_OK && slots >= 8LL * mc) return Ct;
+  }
+  return stream_plan_C(dev, bf16, row_bytes, slots, C);
+}
+
 }  // namespace
 
 extern "C" {
@@ -326,7 +338,7 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
   const int E = static_cast<int>(16 / es);
   const long long slots = static_cast<long long>(B) * N;
   P.units = V / E;
-  P.C = stream_plan_C(dev, bf16, static_cast<long long>(V) * static_cast<long long>(es), slots, sC);
+  P.C = tree_plan_C(dev, bf16, static_cast<long long>(V) * static_cast<long long>(es), slots, sC);
   P.per = (P.units + P.C - 1) / P.C;
   int maxc = 0;
   if (max_clusters(dev, bf16, P.C, &maxc) != SV_OK) return SV_ERR_CUDA;
