@@ -95,6 +95,33 @@ def test_argument_errors_are_host_side(L):
     assert call(L, dtype=0, V=65539) == 2
 
 
+def call_filtered(L, **kw):
+    B, G, V, dtype = kw.get("B", 2), kw.get("G", 3), kw.get("V", 256), kw.get("dtype", 1)
+    args = dict(zt=FAKE, zd=FAKE + 4096, tok=FAKE + 8192, dl=FAKE + 12288, T=FAKE + 16384,
+                tk=FAKE + 17408, tp=FAKE + 18432, u=FAKE + 20480, ot=FAKE + 24576,
+                on=FAKE + 28672, oa=FAKE + 32768, ws=FAKE + 65536, wsb=1 << 20)
+    args.update({k: v for k, v in kw.items() if k in args})
+    return L.spec_verify_filtered(args["zt"], args["zd"], args["tok"], args["dl"], args["T"],
+                                  args["tk"], args["tp"], args["u"], args["ot"], args["on"],
+                                  args["oa"], None, None, B, G, V, dtype, args["ws"], args["wsb"],
+                                  None)
+
+
+def test_filtered_argument_errors_are_host_side(L):
+    """spec_verify_filtered checks everything before it touches the device (16-byte rows only)."""
+    assert call_filtered(L, dtype=5) == 3             # SV_ERR_BAD_DTYPE
+    assert call_filtered(L, B=0) == 2                 # SV_ERR_BAD_SHAPE
+    assert call_filtered(L, G=65) == 2
+    assert call_filtered(L, zt=None) == 1             # SV_ERR_NULL_POINTER
+    assert call_filtered(L, zd=None) == 1
+    assert call_filtered(L, tk=FAKE + 17409) == 5     # SV_ERR_MISALIGNED: top_k needs 4 B
+    assert call_filtered(L, tp=FAKE + 18434) == 5     # top_p needs 4 B
+    assert call_filtered(L, zt=FAKE + 8) == 5         # logit bases need 16 B here
+    assert call_filtered(L, V=257) == 2               # 514-byte rows: not a multiple of 16
+    assert call_filtered(L, ws=None) == 4             # SV_ERR_WORKSPACE_TOO_SMALL
+    assert call_filtered(L, V=16 * 65536 + 8) == 2    # more than 16 chunks of the row buffer
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import speculative_decoding_verification_55_gb300._binding as b
     monkeypatch.setattr(b, "_lib", None)
