@@ -122,6 +122,59 @@ def test_filtered_argument_errors_are_host_side(L):
     assert call_filtered(L, V=16 * 65536 + 8) == 2    # more than 16 chunks of the row buffer
 
 
+def test_tree_onehot_rollback_argument_errors_are_host_side(L):
+    """The tree, one-hot and rollback entry points reject bad arguments before any device call."""
+    def tree(**kw):
+        a = dict(zt=FAKE, tok=FAKE + 4096, par=FAKE + 8192, size=None, path=FAKE + 12288,
+                 plen=FAKE + 16384, otok=FAKE + 20480, pred=None, ws=FAKE + 65536, wsb=1 << 20,
+                 B=2, N=7, V=256, dtype=1)
+        a.update(kw)
+        return L.spec_verify_tree_greedy(a["zt"], a["tok"], a["par"], a["size"], a["path"],
+                                         a["plen"], a["otok"], a["pred"], a["B"], a["N"], a["V"],
+                                         a["dtype"], a["ws"], a["wsb"], None)
+
+    assert tree(dtype=5) == 3
+    assert tree(N=0) == 2 and tree(N=66) == 2          # N - 1 drafted levels at most SV_MAX_GAMMA
+    assert tree(zt=None) == 1 and tree(par=None) == 1 and tree(path=None) == 1
+    assert tree(tok=FAKE + 4097) == 5
+    assert tree(ws=None) == 4
+    assert tree(V=257) == 2                            # 514-byte rows: streaming kernel only
+    assert tree(zt=FAKE + 8) == 5                      # row bases need 16 B
+
+    def onehot(**kw):
+        a = dict(zt=FAKE, tok=FAKE + 8192, dl=FAKE + 12288, T=FAKE + 16384, u=FAKE + 20480,
+                 ot=FAKE + 24576, on=FAKE + 28672, oa=FAKE + 32768, ws=FAKE + 65536, wsb=1 << 20,
+                 B=2, G=3, V=256, dtype=1)
+        a.update(kw)
+        return L.spec_verify_onehot(a["zt"], a["tok"], a["dl"], a["T"], a["u"], a["ot"], a["on"],
+                                    a["oa"], None, None, a["B"], a["G"], a["V"], a["dtype"], a["ws"],
+                                    a["wsb"], None)
+
+    assert onehot(dtype=5) == 3
+    assert onehot(B=0) == 2
+    assert onehot(tok=None) == 1                       # drafted tokens are needed when G > 0
+    assert onehot(T=FAKE + 16385) == 5
+    assert onehot(ws=None) == 4
+    assert onehot(V=257) == 2                          # one-hot drafts: streaming kernel only
+    assert onehot(zt=FAKE + 8) == 5
+
+    def rollback(**kw):
+        a = dict(pre=FAKE, dl=None, num=FAKE + 4096, din=None, tout=FAKE + 8192, dout=None,
+                 cache=None, stride=0, eb=0, ne=0, B=2, G=3)
+        a.update(kw)
+        return L.spec_verify_kv_rollback(a["pre"], a["dl"], a["num"], a["din"], a["tout"],
+                                         a["dout"], a["cache"], a["stride"], a["eb"], a["ne"],
+                                         a["B"], a["G"], None)
+
+    assert rollback(B=0) == 2 and rollback(G=65) == 2
+    assert rollback(pre=None) == 1 and rollback(num=None) == 1 and rollback(tout=None) == 1
+    assert rollback(num=FAKE + 4098) == 5
+    assert rollback(cache=FAKE + 65536, eb=0, ne=4, stride=1024) == 2      # no entry size
+    assert rollback(cache=FAKE + 65536, eb=256, ne=8, stride=1024) == 2    # stride < 8 entries
+    assert rollback(cache=FAKE + 65536, eb=24, ne=4, stride=1024) == 5     # entries of 16 B
+    assert rollback(cache=FAKE + 65544, eb=256, ne=4, stride=1024) == 5    # cache base 16 B
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import speculative_decoding_verification_55_gb300._binding as b
     monkeypatch.setattr(b, "_lib", None)
