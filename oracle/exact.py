@@ -29,8 +29,12 @@ def residual(p, q):
 
 
 def accept_prob(p_x, q_x):
-    """min(1, p(x)/q(x)) (rayaq.ca, One round, step 3)."""
-    return Fraction(1) if q_x == 0 else min(Fraction(1), Fraction(p_x) / Fraction(q_x))
+    """min(1, p(x)/q(x)) (rayaq.ca, One round, step 3). With q(x) = 0: 1 when p(x) > 0, 0 when
+    p(x) = 0 (a token of zero target mass is never emitted: rayaq.ca, The output distribution is
+    exactly the target's)."""
+    if q_x == 0:
+        return Fraction(1) if p_x > 0 else Fraction(0)
+    return min(Fraction(1), Fraction(p_x) / Fraction(q_x))
 
 
 def round_outcomes(p_next, q_next, start, gamma):

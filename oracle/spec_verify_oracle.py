@@ -41,7 +41,8 @@ Readings where the pages leave a step open (each repeated in the design notes):
   If rounding leaves no prefix above the threshold, the last token with w > 0 is taken.
 * A residual with zero total mass at a rejection (impossible in exact arithmetic) falls back to a
   bonus-style draw from that position's p with ``u[b, G]``.
-* q(x) = 0 for a drafted x gives ratio 1 (accept).
+* q(x) = 0 for a drafted x gives ratio 1 (accept) when p(x) > 0, and ratio 0 (reject) when
+  p(x) = 0 as well.
 * Greedy rows are the rows with temperature exactly 0. Argmax ties go to the lowest index. Greedy
   alpha_i = [x_i == g_i], p(x_i) = [x_i == g_i], q(x_i) = 1 (one-hot p and one-hot drafter).
 * alpha_i, p_i(x_i), q_i(x_i) are reported for every i < gamma_b, also after the first rejection;
@@ -113,9 +114,11 @@ def filtered_softmax(z, T, top_k=0, top_p=1.0):
 
 def accept_ratio(p_x, q_x):
     """min(1, p(x)/q(x)) ([R] One round, step 3; [C] The correction that makes it exact).
-    q(x) = 0 reads as ratio 1: a token the drafter proposed with zero mass is kept."""
+    q(x) = 0 (a token the drafter gave no mass, e.g. a -inf draft logit) reads as ratio 1 when
+    p(x) > 0 (p >= q is always kept) and as ratio 0 when p(x) = 0 too: a token the target gives no
+    mass is never emitted ([R] The output distribution is exactly the target's)."""
     if q_x <= 0.0:
-        return 1.0
+        return 1.0 if p_x > 0.0 else 0.0
     return min(1.0, p_x / q_x)
 
 

@@ -89,6 +89,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// The accept probability min(1, p(x)/q(x)) ([R] One round, step 3). q(x) = 0 gives 1 when p(x) > 0
+// (p >= q is always kept) and 0 when p(x) = 0 as well: a token the target gives no mass is never
+// emitted ([R] The output distribution is exactly the target's). Round-to-nearest division.
+__device__ __forceinline__ float accept_ratio(float px, float qx) {
+  if (qx > 0.0f) return fminf(1.0f, __fdiv_rn(px, qx));
+  return px > 0.0f ? 1.0f : 0.0f;
+}
+
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));

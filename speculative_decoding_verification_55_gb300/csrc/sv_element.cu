@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, (VPT <= 4 ? 2 : 1)) sv_element_kerne
       const float zx_d = load_logit<BF16>(rowd, x);
       px = __fdiv_rn(scaled_exp(zx_t, Mt, k), St);
       qx = __fdiv_rn(scaled_exp(zx_d, Md, k), Sd);
-      const float ratio = (qx > 0.0f) ? fminf(1.0f, __fdiv_rn(px, qx)) : 1.0f;
+      const float ratio = accept_ratio(px, qx);
       acc = __ldg(ur + i) < ratio;
 
       // ---- Phase C: alpha = sum min(p, q) and residual mass sum max(0, p - q) ----

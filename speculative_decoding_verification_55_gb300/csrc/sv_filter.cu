@@ -977,7 +977,7 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
             if (p.two) {
               px = wt_l(e_zt);
               qx = wd_l(e_zd);
-              const float ratio = (qx > 0.0f) ? fminf(1.0f, px / qx) : 1.0f;
+              const float ratio = accept_ratio(px, qx);
               acc = e_uacc < ratio ? 1.0f : 0.0f;
             }
             const int run = (N0 + 31) / 32;
@@ -1199,7 +1199,7 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
     if (p.two && !bad) {
       px = wt_of(load_logit<BF16>(rowt, x));
       qx = wd_of(load_logit<BF16>(rowd, x));
-      const float ratio = (qx > 0.0f) ? fminf(1.0f, px / qx) : 1.0f;
+      const float ratio = accept_ratio(px, qx);
       acc = __ldg(P.uniforms + (size_t)p.b * (G + 2) + p.i) < ratio ? 1.0f : 0.0f;
     }
     float wsum = 0.0f, psum = 0.0f;

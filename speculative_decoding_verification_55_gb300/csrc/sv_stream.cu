@@ -576,10 +576,11 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
           sm.acc = 1;
           sm.px = sm.qx = 0.0f;
           if (kind == kVerify) {
-            // [R] One round, step 3: keep x while u < min(1, p(x)/q(x)); q(x) = 0 keeps x.
+            // [R] One round, step 3: keep x while u < min(1, p(x)/q(x)); q(x) = 0 keeps x when
+            // p(x) > 0 and rejects it when p(x) = 0 too (zero target mass is never emitted).
             const float px = ex2(fmaf(zx_t, k, ct));
             const float qx = ex2(fmaf(zx_d, k, cd));
-            const float ratio = (qx > 0.0f) ? fminf(1.0f, __fdividef(px, qx)) : 1.0f;
+            const float ratio = accept_ratio(px, qx);
             sm.px = px;
             sm.qx = qx;
             sm.acc = u_acc < ratio;

@@ -300,6 +300,41 @@ def test_gpu_filtered_ties_and_degenerate_rows(sv, dtype):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gpu_filtered_token_outside_both_kept_sets(sv, dtype):
+    """A drafted token that top-k leaves out of both the filtered p and q has p~(x) = q~(x) = 0: it is
+    rejected and never emitted ([R] Why the output is exactly the target's: the filters are applied
+    to p and q alike; The output distribution is exactly the target's). Rows 0-3 draft such a
+    token; rows 4-7 draft the largest logit (kept by both)."""
+    B, G, V = 8, 2, 4096
+    rng = np.random.default_rng(77)
+    zt = (rng.standard_normal((B, G + 1, V)) * 2.0).astype(np.float32)
+    zd = (zt[:, :G] + rng.standard_normal((B, G, V)).astype(np.float32) * 0.3).astype(np.float32)
+    if dtype == "bf16":
+        zt, zd = bf16_round(zt), bf16_round(zd)
+    T = np.ones(B, np.float32)
+    n = np.full(B, G, np.int32)
+    top_k = np.full(B, 20, np.int32)
+    top_p = np.ones(B, np.float32)
+    u = rng.random((B, G + 2), dtype=np.float32)
+    u[:, :G] = 0.5                          # far from the zero ratio: an exact decision
+    x = np.zeros((B, G), np.int32)
+    for b in range(B):
+        for i in range(G):
+            if b < 4:                       # the smallest logit of both rows: outside both top-20 sets
+                x[b, i] = int(np.argmin(zt[b, i] + zd[b, i]))
+            else:
+                x[b, i] = int(np.argmax(zd[b, i]))
+    o = oracle_verify(zt, zd, x, n, T, u, diagnostics=True, top_k=top_k, top_p=top_p)
+    gpu = run_filtered(sv, zt, zd, x, n, T, u, top_k, top_p, dtype)
+    rep = compare(o, *gpu, x, n)
+    assert rep.ok(), str(rep)
+    for b in range(4):
+        assert o.rows[b].k == 0 and gpu[1][b] == 1 and gpu[0][b, 0] != x[b, 0]
+        assert gpu[3][b, 0] == 0.0 and gpu[4][b, 0] == 0.0
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("dtype,V", [("bf16", 100000), ("f32", 40000)])
 def test_gpu_filtered_candidate_lists(sv, dtype, V):
     """Top-k rows whose candidates (every logit in the value bin of the k-th largest or above) are

@@ -154,7 +154,10 @@ def test_quiz_ratio_and_kept_when_p_ge_q():
         assert accept_ratio(item["p"], item["q"]) == pytest.approx(item["value"], abs=1e-15)
     assert accept_ratio(0.5, 0.2) == 1.0
     assert accept_ratio(0.3, 0.3) == 1.0
-    assert accept_ratio(0.0, 0.0) == 1.0   # q(x) = 0 reading: ratio 1
+    # q(x) = 0 reading: kept when the target gives x mass, rejected when it gives none (a token of
+    # zero target mass is never emitted: [R] The output distribution is exactly the target's)
+    assert accept_ratio(0.25, 0.0) == 1.0
+    assert accept_ratio(0.0, 0.0) == 0.0
 
 
 def test_expected_tokens_closed_form_matches_pages():
@@ -401,15 +404,41 @@ def test_zero_draft_length():
     assert r.out_tokens[0, 0] == inverse_cdf(p, np.float64(u[0, 4]))
 
 
-def test_verify_row_residual_fallback_zero_mass():
-    """A rejection whose residual has zero mass draws from p with the residual uniform."""
-    V = 4
-    p = np.array([0.25, 0.25, 0.25, 0.25])
-    zt = np.log(np.stack([p, p]))
-    # q(x) slightly above p(x) forces ratio < 1, but the residual mass is what rounding leaves
-    res = verify_row(zt, zt[:1], np.asarray([1]), 1, np.float32(1.0),
-                     np.asarray([0.9999999, 0.6, 0.3], np.float32), 1)
-    assert res.k == 1   # equal rows: ratio exactly 1, always accepted
+def zero_residual_row(V, x=3, seed=3, dtype=np.float32):
+    """One drafted position whose fp64 residual max(0, p - q) has zero total mass although
+    p(x) < q(x): every logit but x's is the same in both rows, and x's logit (-40 in the target, -39
+    in the draft) is so small that its term vanishes in both normalisers. So p and q agree exactly
+    everywhere but at x, where p(x)/q(x) = e^-1. (In exact arithmetic the residual is p without x,
+    whose draw matches the fallback's draw from p.) Returns (zt [2, V], zd [1, V], x)."""
+    rng = np.random.default_rng(seed)
+    base = np.abs(rng.standard_normal(V)).astype(dtype)
+    zt, zd = base.copy(), base.copy()
+    zt[x], zd[x] = -40.0, -39.0
+    return np.stack([zt, base]), zd[None], x
+
+
+@pytest.mark.parametrize("V", [8, 64, 4096])
+def test_verify_row_residual_fallback_zero_mass(V):
+    """A rejection whose residual has zero mass draws from that position's p with the residual
+    uniform u[G] (the reading for a step the pages leave open: [R] One round, step 4 cannot divide
+    by a zero mass). The case is a real one: fp64 rounding leaves the residual exactly empty."""
+    zt, zd, x = zero_residual_row(V)
+    p = temperature_softmax(zt[0], 1.0)
+    q = temperature_softmax(zd[0], 1.0)
+    assert np.sum(residual_weights(p, q)) == 0.0          # the fallback's condition, reached
+    assert p[x] < q[x]
+    assert accept_ratio(p[x], q[x]) == pytest.approx(np.exp(-1.0), rel=1e-12)
+    u = np.array([0.9, 0.05, 0.81], np.float32)          # u[0] rejects; u[G] = 0.05; u[G+1] = 0.81
+    res = verify_row(zt, zd, np.asarray([x]), 1, np.float32(1.0), u, 1, diagnostics=True)
+    assert res.k == 0
+    want = inverse_cdf(p, np.float64(u[1]))
+    assert res.tokens == [want]
+    # the mistakes this branch could hide give other tokens on this row
+    assert want != inverse_cdf(p, np.float64(u[2]))                 # the bonus uniform
+    assert want != int(np.flatnonzero(p > 0)[-1])                   # the last token
+    assert want != int(np.argmax(p))                                 # the mode
+    assert want != x                                                  # the rejected draft
+    assert res.exact
 
 
 def test_accept_is_strict_at_the_ratio():

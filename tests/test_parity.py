@@ -221,6 +221,70 @@ def test_zero_draft_mass_and_equal_rows(sv):
     assert (gpu[1] == G + 1).all()
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [7, 64, 4096, 65536])
+def test_zero_residual_mass_fallback(sv, dtype, V):
+    """A rejection whose residual max(0, p - q) has zero mass draws from p with u[G], the reading
+    the oracle takes for a step the pages leave open ([R] One round, step 4). The rows of
+    zero_residual_row reach it in fp64 and in the kernels' fp32 alike: x's logit (-40 target, -39
+    draft) vanishes in both normalisers, so p = q away from x and p(x) = q(x) / e. V = 7 runs on
+    the element path, the others on the streaming path."""
+    from test_oracle import zero_residual_row
+    B, G = 6, 1
+    zt = np.zeros((B, G + 1, V), np.float32)
+    zd = np.zeros((B, G, V), np.float32)
+    tokens = np.zeros((B, G), np.int32)
+    for b in range(B):
+        x = (3 + 5 * b) % V
+        a, d, _ = zero_residual_row(V, x=x, seed=b)
+        zt[b], zd[b], tokens[b, 0] = a, d, x
+    if dtype == "bf16":
+        zt, zd = bf16_round(zt), bf16_round(zd)
+    u = np.tile(np.array([0.9, 0.05, 0.81], np.float32), (B, 1))
+    u[:, 1] = np.linspace(0.05, 0.95, B, dtype=np.float32)        # a spread of residual uniforms
+    args = (zt, zd, tokens, np.ones(B, np.int32), np.ones(B, np.float32), u)
+    o = oracle_verify(*args, diagnostics=True)
+    for b in range(B):                       # the oracle takes the fallback on every row
+        p = o.rows[b]
+        assert p.k == 0 and p.ratio[0] == pytest.approx(np.exp(-1.0), rel=1e-9)
+    gpu = run_gpu(sv, to_dev(*args, dtype))
+    rep = check(o, gpu, tokens, args[3])
+    assert rep.exact_rows >= B - 1, str(rep)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_mass_drafted_token_is_rejected(sv, dtype):
+    """A drafted token that both p and q give zero mass (-inf in both logit rows) is rejected and
+    never emitted ([R] The output distribution is exactly the target's); a token with q(x) = 0 and
+    p(x) > 0 is kept. Streaming path (V = 4096) and element path (V = 1001)."""
+    for V in (4096, 1001):
+        B, G = 8, 3
+        rng = np.random.default_rng(V)
+        zt = rng.normal(0, 2, (B, G + 1, V)).astype(np.float32)
+        zd = (zt[:, :G] + rng.normal(0, 0.5, (B, G, V))).astype(np.float32)
+        tokens = rng.integers(0, V, (B, G)).astype(np.int32)
+        for b in range(B):
+            i = b % G
+            zd[b, i, tokens[b, i]] = -np.inf
+            if b < B // 2:                     # rows 0-3: p(x) = 0 too
+                zt[b, i, tokens[b, i]] = -np.inf
+        if dtype == "bf16":
+            zt, zd = bf16_round(zt), bf16_round(zd)
+        u = rng.random((B, G + 2), dtype=np.float32)
+        u[:, :G] = 1e-4                        # other drafts kept; the zero ratio rejects, exactly
+        args = (zt, zd, tokens, np.full(B, G, np.int32), np.ones(B, np.float32), u)
+        o = oracle_verify(*args, diagnostics=True)
+        gpu = run_gpu(sv, to_dev(*args, dtype))
+        check(o, gpu, tokens, args[3])
+        for b in range(B):
+            i = b % G
+            if b < B // 2:
+                assert gpu[1][b] == i + 1 and gpu[0][b, i] != tokens[b, i], b
+                assert gpu[3][b, i] == 0.0 and gpu[4][b, i] == 0.0
+            else:                              # q(x) = 0 < p(x): ratio 1, never the rejection
+                assert gpu[1][b] - 1 != i, b
+
+
 @pytest.mark.parametrize("case", ["len_neg", "len_big", "T_nan", "T_neg", "T_inf", "T_subnormal",
                                   "tok_neg", "tok_big", "u_one", "u_nan", "nan_logit",
                                   "pinf_logit", "all_ninf", "draft_nan", "greedy_nan"])
