@@ -244,11 +244,15 @@ int spec_verify_kv_rollback(const int32_t* prefix_len, const int32_t* draft_len,
  *
  * Limit: sizes whose spec_verify_workspace_size(B, gamma_max, V, dtype) exceeds
  * SV_NOALLOC_SCRATCH_BYTES are rejected with SV_ERR_SCRATCH_TOO_SMALL before anything is enqueued.
+ * Every other argument is checked as spec_verify_ex checks it, also before anything is enqueued,
+ * and a rejected call returns the status spec_verify_ex would return.
  * Set-up: the first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture. Each call clears the
- * scratch's counters on `cuda_stream` before its launch. Every call shares the one array: calls
- * whose executions overlap on the GPU (other streams, other host threads) race and must be
- * serialised by the caller. Arguments, layout and errors otherwise as in spec_verify_ex. */
+ * with the current device, which must be the device of the buffers; make that first call before
+ * any stream capture. Each call then clears the part of the array it uses (records, row counters
+ * and status word: spec_verify_workspace_size bytes) on `cuda_stream` before its launch, so a
+ * call never sees what an earlier one left. Every call shares the one array: calls whose
+ * executions overlap on the GPU (other streams, other host threads) race and must be serialised
+ * by the caller. Arguments, layout and errors otherwise as in spec_verify_ex. */
 int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
                         const int32_t* draft_tokens, const int32_t* draft_len,
                         const float* temperature, const float* uniforms, int32_t* out_tokens,

@@ -100,8 +100,9 @@ def spec_verify_status_string(status: int) -> str:
 def spec_verify_workspace_status(workspace, B: int, gamma_max: int, stream=None) -> int:
     """The workspace's sticky status word (0 = every call completed its protocol)."""
     out = ctypes.c_int32(0)
-    st = lib().spec_verify_workspace_status(_ptr(workspace), B, gamma_max, ctypes.byref(out),
-                                            _stream_handle(stream, workspace.device))
+    with _on(workspace.device):
+        st = lib().spec_verify_workspace_status(_ptr(workspace), B, gamma_max, ctypes.byref(out),
+                                                _stream_handle(stream, workspace.device))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_workspace_status")
     return int(out.value)
@@ -141,6 +142,16 @@ def _check(t, name, dtype=None, shape=None, device=None):
         raise ValueError(f"{name} must be on {device}, got {t.device}")
 
 
+def _on(device):
+    """The CUDA device of the call's buffers made current for the C call: the library launches on
+    (and, for spec_verify_noalloc, takes the scratch address of) the current device."""
+    import contextlib
+    import torch
+    if device is None or device.type != "cuda":
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def _stream_handle(stream, device):
     import torch
     if stream is None:
@@ -170,12 +181,13 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, tempera
         _check(t, name, torch.float32, (B, G), dev)
     _check(workspace, "workspace", device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().spec_verify_ex(
-        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
-        _ptr(temperature), _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted),
-        _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
-        B, G, V, _dtype_code(target_logits), _ptr(workspace), ws_bytes,
-        _stream_handle(stream, dev))
+    with _on(dev):
+        st = lib().spec_verify_ex(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
+            _ptr(temperature), _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted),
+            _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
+            B, G, V, _dtype_code(target_logits), _ptr(workspace), ws_bytes,
+            _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_ex")
 
@@ -226,12 +238,13 @@ def spec_verify_staged(target_logits, draft_logits, draft_tokens, draft_len, tem
     dev = staging.device
     _check(workspace, "workspace", device=dev)
     n = ctypes.c_size_t(0)
-    st = lib().spec_verify_staged(
-        _host_ptr(target_logits), _host_ptr(draft_logits), _host_ptr(draft_tokens),
-        _host_ptr(draft_len), _host_ptr(temperature), _host_ptr(uniforms), _host_ptr(out_tokens),
-        _host_ptr(out_num_emitted), _host_ptr(out_alpha), B, G, V, _dtype_code(target_logits),
-        _ptr(staging), staging.numel() * staging.element_size(), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), ctypes.byref(n), _stream_handle(stream, dev))
+    with _on(dev):
+        st = lib().spec_verify_staged(
+            _host_ptr(target_logits), _host_ptr(draft_logits), _host_ptr(draft_tokens),
+            _host_ptr(draft_len), _host_ptr(temperature), _host_ptr(uniforms), _host_ptr(out_tokens),
+            _host_ptr(out_num_emitted), _host_ptr(out_alpha), B, G, V, _dtype_code(target_logits),
+            _ptr(staging), staging.numel() * staging.element_size(), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), ctypes.byref(n), _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_staged")
     return int(n.value)
@@ -285,11 +298,12 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, draft_len, te
     for name, t in (("out_alpha", out_alpha), ("out_p_draft", out_p_draft),
                     ("out_q_draft", out_q_draft)):
         _check(t, name, torch.float32, (B, G), dev)
-    st = lib().spec_verify_noalloc(
-        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
-        _ptr(temperature), _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted),
-        _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
-        B, G, V, _dtype_code(target_logits), _stream_handle(stream, dev))
+    with _on(dev):
+        st = lib().spec_verify_noalloc(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
+            _ptr(temperature), _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted),
+            _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
+            B, G, V, _dtype_code(target_logits), _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_noalloc")
 
@@ -315,11 +329,12 @@ def spec_verify_onehot(target_logits, draft_tokens, draft_len, temperature, unif
         _check(t, name, torch.float32, (B, G), dev)
     _check(workspace, "workspace", device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().spec_verify_onehot(
-        _ptr(target_logits), _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature),
-        _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted), _ptr(out_alpha),
-        _ptr(out_p_draft), _ptr(out_q_draft), B, G, V, _dtype_code(target_logits),
-        _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    with _on(dev):
+        st = lib().spec_verify_onehot(
+            _ptr(target_logits), _ptr(draft_tokens), _ptr(draft_len), _ptr(temperature),
+            _ptr(uniforms), _ptr(out_tokens), _ptr(out_num_emitted), _ptr(out_alpha),
+            _ptr(out_p_draft), _ptr(out_q_draft), B, G, V, _dtype_code(target_logits),
+            _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_onehot")
 
@@ -349,12 +364,13 @@ def spec_verify_filtered(target_logits, draft_logits, draft_tokens, draft_len, t
         _check(t, name, torch.float32, (B, G), dev)
     _check(workspace, "workspace", device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().spec_verify_filtered(
-        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
-        _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(out_tokens),
-        _ptr(out_num_emitted), _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
-        B, G, V, _dtype_code(target_logits), _ptr(workspace), ws_bytes,
-        _stream_handle(stream, dev))
+    with _on(dev):
+        st = lib().spec_verify_filtered(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(draft_len),
+            _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(uniforms), _ptr(out_tokens),
+            _ptr(out_num_emitted), _ptr(out_alpha), _ptr(out_p_draft), _ptr(out_q_draft),
+            B, G, V, _dtype_code(target_logits), _ptr(workspace), ws_bytes,
+            _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_filtered")
 
@@ -376,10 +392,11 @@ def spec_verify_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size,
     _check(out_pred, "out_pred", torch.int32, (B, N), dev)
     _check(workspace, "workspace", device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().spec_verify_tree_greedy(
-        _ptr(target_logits), _ptr(tree_tokens), _ptr(tree_parents), _ptr(tree_size),
-        _ptr(out_path), _ptr(out_path_len), _ptr(out_tokens), _ptr(out_pred), B, N, V,
-        _dtype_code(target_logits), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
+    with _on(dev):
+        st = lib().spec_verify_tree_greedy(
+            _ptr(target_logits), _ptr(tree_tokens), _ptr(tree_parents), _ptr(tree_size),
+            _ptr(out_path), _ptr(out_path_len), _ptr(out_tokens), _ptr(out_pred), B, N, V,
+            _dtype_code(target_logits), _ptr(workspace), ws_bytes, _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_tree_greedy")
 
@@ -403,10 +420,11 @@ def spec_verify_kv_rollback(prefix_len, draft_len, out_num_emitted, drafter_len_
         entries = cache.shape[1]
         entry = cache[0, 0].numel() * cache.element_size()
         stride = cache[0].numel() * cache.element_size()
-    st = lib().spec_verify_kv_rollback(
-        _ptr(prefix_len), _ptr(draft_len), _ptr(out_num_emitted), _ptr(drafter_len_in),
-        _ptr(target_len_out), _ptr(drafter_len_out), _ptr(cache), stride, entry, entries, B,
-        gamma_max, _stream_handle(stream, dev))
+    with _on(dev):
+        st = lib().spec_verify_kv_rollback(
+            _ptr(prefix_len), _ptr(draft_len), _ptr(out_num_emitted), _ptr(drafter_len_in),
+            _ptr(target_len_out), _ptr(drafter_len_out), _ptr(cache), stride, entry, entries, B,
+            gamma_max, _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_kv_rollback")
 

@@ -198,7 +198,8 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
                 int32_t* out_tokens, int32_t* out_num_emitted, float* out_alpha,
                 float* out_p_draft, float* out_q_draft,
                 int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
-                void* workspace, size_t workspace_bytes, void* cuda_stream, bool onehot) {
+                void* workspace, size_t workspace_bytes, void* cuda_stream, bool onehot,
+                bool check_only = false) {
   if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
   if (!sizes_ok(B, gamma_max, V, dtype)) return SV_ERR_BAD_SHAPE;
   const int G = gamma_max;
@@ -213,7 +214,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
       mis(out_alpha, 4) || mis(out_p_draft, 4) || mis(out_q_draft, 4) || mis(workspace, 16))
     return SV_ERR_MISALIGNED;
   const size_t need = spec_verify_workspace_size(B, G, V, dtype);
-  if (!workspace || workspace_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
+  if (!check_only && (!workspace || workspace_bytes < need)) return SV_ERR_WORKSPACE_TOO_SMALL;
   if (static_cast<long long>(B) * (G + 1) > INT_MAX / sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
 
   const bool vec = (static_cast<size_t>(V) * es) % 16 == 0 &&
@@ -229,7 +230,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
 
   int dev = 0;
   const int dev_status = check_device(&dev);
-  if (dev_status != SV_OK) return dev_status;
+  if (dev_status != SV_OK || check_only) return dev_status;
 
   sv::Params P{};
   P.onehot = onehot ? 1 : 0;
@@ -275,6 +276,20 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
 }
 
 }  // namespace
+
+namespace sv {
+
+int verify_args_status(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const int32_t* draft_len,
+                       const float* temperature, const float* uniforms, int32_t* out_tokens,
+                       int32_t* out_num_emitted, float* out_alpha, float* out_p_draft,
+                       float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype) {
+  return verify_impl(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                     out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft, B, gamma_max,
+                     V, dtype, nullptr, 0, nullptr, false, true);
+}
+
+}  // namespace sv
 
 extern "C" {
 

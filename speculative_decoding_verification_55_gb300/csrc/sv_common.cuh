@@ -719,6 +719,14 @@ __device__ __forceinline__ bool earlier_rejection(const Params& P, int b, int i,
 // Host-side launchers (defined in the kernel translation units)
 // ------------------------------------------------------------------------------------------------
 
+// Every check spec_verify_ex makes before it enqueues anything (sizes, dtype, pointers, alignment,
+// the row layout, the device), without the workspace: the status it would return, or SV_OK.
+int verify_args_status(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const int32_t* draft_len,
+                       const float* temperature, const float* uniforms, int32_t* out_tokens,
+                       int32_t* out_num_emitted, float* out_alpha, float* out_p_draft,
+                       float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
+
 // Element path (any alignment, V <= 16 * 512 * 8): one cluster per position slot.
 cudaError_t launch_element(const Params& P, bool bf16, int vpt_index, cudaStream_t stream);
 // Streaming path (16-byte aligned rows): persistent clusters fed by bulk copies.

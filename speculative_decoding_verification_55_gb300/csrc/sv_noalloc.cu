@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "../../include/spec_verify.h"
+#include "sv_common.cuh"
 
 namespace {
 
@@ -25,8 +26,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRA
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64];                 // device address of the array, per device (set-up done)
-
-size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // Set-up for the current device: the array's device address, looked up once per device.
 int noalloc_scratch(void** out) {
@@ -57,16 +56,21 @@ extern "C" int spec_verify_noalloc(const void* target_logits, const void* draft_
     return SV_ERR_BAD_SHAPE;
   }
   if (need > SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_SCRATCH_TOO_SMALL;
+  // The checks spec_verify_ex makes, first: a rejected call enqueues nothing and returns the status
+  // spec_verify_ex would return.
+  const int args = sv::verify_args_status(target_logits, draft_logits, draft_tokens, draft_len,
+                                          temperature, uniforms, out_tokens, out_num_emitted,
+                                          out_alpha, out_p_draft, out_q_draft, B, gamma_max, V,
+                                          dtype);
+  if (args != SV_OK) return args;
   void* scratch = nullptr;
   const int st = noalloc_scratch(&scratch);
   if (st != SV_OK) return st;
-  // The counters and the status word must start at zero; the array keeps whatever the previous
-  // call left, so clear them on the caller's stream before the launch.
-  const size_t counters_at = align256(static_cast<size_t>(B) * (gamma_max + 1) * 8);
-  char* zero_from = static_cast<char*>(scratch) + counters_at;
+  // The array keeps whatever the previous call left: per-position records, row counters and the
+  // status word must start at zero, and a call that gave up part-way leaves stale records. Clear
+  // this call's whole layout on the caller's stream before the launch.
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
-  if (cudaMemsetAsync(zero_from, 0, static_cast<size_t>(B) * 4 + 4, stream) != cudaSuccess)
-    return SV_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, need, stream) != cudaSuccess) return SV_ERR_CUDA;
   return spec_verify_ex(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
                         out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft, B,
                         gamma_max, V, dtype, scratch, SV_NOALLOC_SCRATCH_BYTES, cuda_stream);

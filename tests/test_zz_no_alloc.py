@@ -35,9 +35,12 @@ def outputs(t, B, G):
             torch.full((B, G), -7.0, dtype=torch.float32, device=dev))
 
 
-def test_noalloc_matches_workspace_entry_point_twice(sv):
+def test_noalloc_matches_workspace_entry_point_and_oracle_twice(sv):
     """Two calls in a row (different batch shapes, so the shared scratch is reused with a new
-    layout) give the same outputs as spec_verify_ex with a caller workspace."""
+    layout) give the same outputs as spec_verify_ex with a caller workspace, and match the fp64
+    oracle under the margin rule of the parity tests."""
+    from _parity import compare
+    from oracle.spec_verify_oracle import oracle_verify
     for key in (2, 3):
         w = make_workload(key)
         t = w.device_tensors()
@@ -52,6 +55,34 @@ def test_noalloc_matches_workspace_entry_point_twice(sv):
         for a, b in zip(out[2:], ref[2:]):
             assert float((a - b).abs().max()) <= TOL, key
         assert int(out[1].min()) >= 1
+        o = oracle_verify(w.target_logits, w.draft_logits, w.draft_tokens, w.draft_len,
+                          w.temperature, w.uniforms, diagnostics=True)
+        rep = compare(o, *[a.cpu().numpy() for a in out], w.draft_tokens, w.draft_len)
+        assert rep.ok(), f"workload {key}: {rep}"
+
+
+def test_noalloc_rejected_call_enqueues_nothing(sv):
+    """A call rejected for a bad argument returns the status spec_verify_ex returns and writes no
+    output (nothing was enqueued)."""
+    w = make_workload(2)
+    t = w.device_tensors()
+    B, G = w.B, w.G
+    ws = sv.workspace_for(B, G, w.V, sv.SV_DTYPE_BF16, t["target_logits"].device)
+    raw = sv.lib()
+    out = outputs(t, B, G)
+    zt = t["target_logits"]
+    args = [zt.data_ptr() + 1, t["draft_logits"].data_ptr(), t["draft_tokens"].data_ptr(),
+            t["draft_len"].data_ptr(), t["temperature"].data_ptr(), t["uniforms"].data_ptr()] + \
+        [o.data_ptr() for o in out]
+    tail = [B, G, w.V, sv.SV_DTYPE_BF16]
+    stream = torch.cuda.current_stream().cuda_stream
+    cases = {"misaligned": args, "null": [None] + args[1:]}
+    for name, a in cases.items():
+        st_ex = raw.spec_verify_ex(*a, *tail, ws.data_ptr(), ws.numel(), stream)
+        st_na = raw.spec_verify_noalloc(*a, *tail, stream)
+        assert st_na == st_ex != 0, (name, st_na, st_ex)
+    torch.cuda.synchronize()
+    assert int((out[1] == -7).sum()) == B and int((out[0] == -7).sum()) == out[0].numel()
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(sv):
