@@ -48,7 +48,10 @@ def parse():
     ap.add_argument("--rows", type=int, default=0, help="use only the first N rows (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="single-core oracle seconds the CPU baseline's row sample is sized for")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the kernel timings of workloads 3 and 4 after the headline")
     ap.add_argument("--onehot", action="store_true",
                     help="one-hot drafts (greedy drafter): time spec_verify_onehot, no draft logits")
     ap.add_argument("--filter", action="store_true",
@@ -206,10 +209,17 @@ def oracle_pool(cfg_key, seconds, seed=12345, onehot=False, filt=False):
     return w, int(np.sum(w.draft_len.astype(np.int64) + 1))
 
 
-def oracle_run(w, onehot=False):
-    """Wall seconds of one oracle pass over the pool's rows."""
+def oracle_run(w, onehot=False, threads=1):
+    """Wall seconds of one oracle pass over the pool's rows (the plain spec_verify rule with
+    threads > 1: rows in parallel threads)."""
     t0 = time.perf_counter()
-    _oracle(w, onehot, getattr(w, "filters", None))
+    if threads > 1 and not onehot and getattr(w, "filters", None) is None:
+        from oracle.spec_verify_oracle import oracle_verify_rows
+        oracle_verify_rows(lambda b: (w.target_logits[b], w.draft_logits[b]), w.draft_tokens,
+                           w.draft_len, w.temperature, w.uniforms, w.G, w.V, range(w.B),
+                           threads=threads)
+    else:
+        _oracle(w, onehot, getattr(w, "filters", None))
     return time.perf_counter() - t0
 
 
@@ -218,6 +228,127 @@ def oracle_sample_rate(cfg_key, seconds, onehot=False, filt=False):
     w, pos = oracle_pool(cfg_key, seconds, onehot=onehot, filt=filt)
     secs = oracle_run(w, onehot)
     return pos / secs, w.B, pos, secs
+
+
+def oracle_threads():
+    """Host cores this process may run on (the all-cores oracle figure uses that many threads)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def cpu_leg(w, gpu_out, seconds, seed=4242):
+    """The oracle, as it stands, on a bounded sample of the timed batch's own rows: timed on one
+    core and on all cores (a thread per core, rows in parallel), then compared with the GPU's
+    outputs for those rows under the margin rule (outside every timed region).
+
+    gpu_out: (out_tokens, out_num, out_alpha) numpy arrays of the timed batch. Returns
+    (cpu_baseline dict, parity dict)."""
+    import numpy as np
+
+    sys.path.insert(0, str(ROOT / "tests"))
+    from _parity import compare
+    from oracle.spec_verify_oracle import oracle_verify_rows
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.B)
+    host = {}
+
+    def source(b):
+        return host[b]
+
+    def run(rows, threads, diagnostics=False):
+        return oracle_verify_rows(source, w.draft_tokens, w.draft_len, w.temperature, w.uniforms,
+                                  w.G, w.V, rows, threads=threads, diagnostics=diagnostics)
+
+    probe = [int(b) for b in order[:4]]
+    for b in probe:
+        host[b] = w.host_rows(b)
+    t0 = time.perf_counter()
+    run(probe, 1)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    n = int(max(4, min(w.B, round(seconds / max(per_row, 1e-6)))))
+    rows = [int(b) for b in order[:n]]
+    for b in rows:
+        if b not in host:
+            host[b] = w.host_rows(b)
+    pos = int(np.sum(w.draft_len[rows].astype(np.int64) + 1))
+    t0 = time.perf_counter()
+    run(rows, 1)
+    t1 = time.perf_counter() - t0
+    cores = oracle_threads()
+    t0 = time.perf_counter()
+    run(rows, cores)
+    tn = time.perf_counter() - t0
+    o = run(rows, cores, diagnostics=True)
+    tok, num, alpha = gpu_out
+    rep = compare(o, tok, num, alpha, None, None, w.draft_tokens, w.draft_len, rows=rows)
+    sample = (f"{n} rows ({pos} positions) of the timed batch, seeded sample, copied back from the "
+              f"device; fp64 oracle, rows in parallel threads")
+    cpu = {"value": pos / tn, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+           "seconds": tn,
+           "single_core": {"value": pos / t1, "unit": UNIT, "cores": 1, "seconds": t1}}
+    parity = dict(rep.as_dict(), sample=f"the same {n} rows", rule="tokens and accept counts "
+                  "bit-exact outside the 1e-5 margin; alpha within 1e-5")
+    return cpu, parity
+
+
+def time_workload(sv, key, steps, warmup, dev, flush_bytes=0):
+    """Kernel time of one spec_verify call on workload `key` (inputs resident in HBM), CUDA events
+    on the launching stream. With flush_bytes, a buffer that large is written between steps (L2
+    flushed) and each step is timed on its own; the mean step time is returned."""
+    import torch
+    from workloads import get_config, make_workload
+    cfg = get_config(key)
+    w = make_workload(cfg, backend="torch", device=dev)
+    t = w.device_tensors(dev)
+    B, G, V = w.B, w.G, w.V
+    dcode = sv.SV_DTYPE_BF16 if cfg.dtype == "bf16" else sv.SV_DTYPE_F32
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.workspace_for(B, G, V, dcode, dev, stream)
+    out = (torch.empty((B, G + 1), dtype=torch.int32, device=dev),
+           torch.empty((B,), dtype=torch.int32, device=dev),
+           torch.empty((B, G), dtype=torch.float32, device=dev))
+
+    def step():
+        sv.spec_verify(t["target_logits"], t["draft_logits"], t["draft_tokens"], t["draft_len"],
+                       t["temperature"], t["uniforms"], *out, ws, stream)
+
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device=dev) if flush_bytes else None
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    times = []
+    if flush is not None:
+        for _ in range(steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(a.elapsed_time(b))
+        ms = sum(times) / len(times)
+    else:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / steps
+    algo = w.algorithmic_bytes()
+    gbs = algo / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    res = {"workload": cfg.name, "ms_per_step": ms, "steps": steps,
+           "positions_per_s": w.positions() / (ms * 1e-3), "algorithmic_bytes_per_step": algo,
+           "achieved_gbs": gbs, "frac": gbs / peak, "peak": peak, "peak_kind": peak_kind,
+           "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+           "l2": (f"{flush_bytes >> 20} MB written between steps" if flush_bytes
+                  else "inputs larger than L2 (no flush)")}
+    del t, w, out, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def workload_name(cfg, args):
@@ -263,11 +394,12 @@ def run_reference(args):
     cfg = get_config(args.workload)
     per_step = 1.5      # seconds of single-thread oracle work per step
     w, pos = oracle_pool(args.workload, per_step, onehot=args.onehot, filt=args.filter)
+    threads = 1 if (args.onehot or args.filter) else oracle_threads()
     for _ in range(args.warmup):
-        oracle_run(w, args.onehot)
+        oracle_run(w, args.onehot, threads)
     total = 0.0
     for _ in range(args.steps):
-        total += oracle_run(w, args.onehot)
+        total += oracle_run(w, args.onehot, threads)
     value = pos * args.steps / total
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -278,9 +410,10 @@ def run_reference(args):
                    "gamma_max": cfg.gamma_max, "V": cfg.V,
                    "logits": cfg.dtype, "sample_rows_per_step": w.B,
                    "sample_positions_per_step": pos},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{w.B} rows ({pos} positions) of the workload drawn on the host "
-                                   f"per step, single-thread fp64 oracle"},
+                                   f"per step, fp64 oracle on {threads} thread(s), rows in "
+                                   f"parallel"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -426,13 +559,29 @@ def run_gpu(args):
                "ms_per_step": ms_e2e, "steps": n_e2e, "path": e2e_path}
         del host, dev_in
 
-    cpu = None
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        rate, rows, pos, secs = oracle_sample_rate(args.workload, args.cpu_seconds, args.onehot,
-                                                   args.filter)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{rows} rows ({pos} positions) of the workload drawn on the host, "
-                         f"{secs:.1f} s of single-thread fp64 oracle work"}
+        if args.onehot or args.filter:
+            rate, rows, pos, secs = oracle_sample_rate(args.workload, args.cpu_seconds,
+                                                       args.onehot, args.filter)
+            cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{rows} rows ({pos} positions) of the workload drawn on the host, "
+                             f"{secs:.1f} s of single-thread fp64 oracle work"}
+        else:
+            step()                   # the timed batch's outputs, once more, for the comparison
+            torch.cuda.synchronize(dev)
+            gpu_out = (out_tokens.cpu().numpy(), out_num.cpu().numpy(), out_alpha.cpu().numpy())
+            cpu, parity = cpu_leg(w, gpu_out, args.cpu_seconds)
+
+    per_config = None
+    if rank == 0 and world == 1 and not (args.onehot or args.filter or args.rows or args.no_per_config):
+        del t
+        torch.cuda.empty_cache()
+        per_config = {}
+        for key, flush in ((3, 256 << 20), (4, 0)):
+            if key != args.workload:
+                per_config[f"workload_{key}"] = time_workload(sv, key, args.steps, args.warmup, dev,
+                                                              flush)
 
     if rank == 0:
         line = {
@@ -457,6 +606,8 @@ def run_gpu(args):
             "clocks": clock_info,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "parity": parity,
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

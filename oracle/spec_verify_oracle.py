@@ -369,6 +369,49 @@ def oracle_verify(target_logits, draft_logits, draft_tokens, draft_len, temperat
     return BatchResult(out_tokens, out_num, out_alpha, out_p, out_q, results)
 
 
+def oracle_verify_rows(row_source, draft_tokens, draft_len, temperature, uniforms, G, V, rows,
+                       threads=1, diagnostics=False, eps=MARGIN):
+    """oracle_verify over the listed rows only, several rows at a time in a pool of threads (numpy
+    releases the interpreter lock inside its array operations). Each row is still verify_row, the
+    plain loop above: the threads change where rows run, not what is computed.
+
+    row_source(b) -> (zt [G+1, V], zd [G, V]) gives a row's stored logits as float arrays; it is
+    called from the pool's threads. Returns a BatchResult of B = len(draft_len) rows whose
+    unlisted rows stay -1 / 0 (rows[b] None)."""
+    from concurrent.futures import ThreadPoolExecutor
+    B = len(draft_len)
+    out_tokens = np.full((B, G + 1), -1, dtype=np.int32)
+    out_num = np.full(B, -1, dtype=np.int32)
+    out_alpha = np.zeros((B, G))
+    out_p = np.zeros((B, G))
+    out_q = np.zeros((B, G))
+    results = [None] * B
+
+    def one(b):
+        zt, zd = row_source(b)
+        return b, verify_row(zt, zd, draft_tokens[b], int(draft_len[b]), np.float32(temperature[b]),
+                             uniforms[b], G, diagnostics=diagnostics, eps=eps)
+
+    if threads <= 1:
+        done = map(one, rows)
+    else:
+        pool = ThreadPoolExecutor(max_workers=threads)
+        done = pool.map(one, rows)
+    try:
+        for b, r in done:
+            results[b] = r
+            if r.valid:
+                out_tokens[b, :len(r.tokens)] = r.tokens
+                out_num[b] = len(r.tokens)
+                out_alpha[b] = r.alpha
+                out_p[b] = r.p_draft
+                out_q[b] = r.q_draft
+    finally:
+        if threads > 1:
+            pool.shutdown()
+    return BatchResult(out_tokens, out_num, out_alpha, out_p, out_q, results)
+
+
 # ----------------------------------------------------------------------------------------------
 # One-hot drafts (a greedy drafter): q_i = [v == x_i]
 # ----------------------------------------------------------------------------------------------

@@ -24,14 +24,33 @@ class ParityReport:
     error_rows: int = 0
     max_alpha_err: float = 0.0
     max_prob_err: float = 0.0
+    positions: int = 0              # verified positions of the compared rows (sum of gamma_b + 1)
+    margin_positions: int = 0       # decisions inside the margin (accept tests and final draws)
     failures: list = field(default_factory=list)
 
     def ok(self):
         return not self.failures
 
+    def merge(self, other):
+        for name in ("rows", "exact_rows", "margin_rows", "error_rows", "positions",
+                     "margin_positions"):
+            setattr(self, name, getattr(self, name) + getattr(other, name))
+        self.max_alpha_err = max(self.max_alpha_err, other.max_alpha_err)
+        self.max_prob_err = max(self.max_prob_err, other.max_prob_err)
+        self.failures += other.failures
+        return self
+
+    def as_dict(self):
+        return {"rows_checked": self.rows, "exact_rows": self.exact_rows,
+                "margin_rows": self.margin_rows, "error_rows": self.error_rows,
+                "positions_checked": self.positions, "margin_positions": self.margin_positions,
+                "max_abs_alpha_err": self.max_alpha_err, "max_abs_prob_err": self.max_prob_err,
+                "failures": len(self.failures)}
+
     def __str__(self):
         return (f"rows={self.rows} exact={self.exact_rows} margin={self.margin_rows} "
-                f"error_rows={self.error_rows} max|dalpha|={self.max_alpha_err:.2e} "
+                f"error_rows={self.error_rows} positions={self.positions} "
+                f"margin_positions={self.margin_positions} max|dalpha|={self.max_alpha_err:.2e} "
                 f"max|dp|={self.max_prob_err:.2e} failures={self.failures[:5]}")
 
 
@@ -52,6 +71,9 @@ def compare(oracle, gpu_tokens, gpu_num, gpu_alpha, gpu_p, gpu_q, draft_tokens, 
                 rep.failures.append((b, "alpha not zeroed on error row"))
             continue
         gb = int(draft_len[b])
+        rep.positions += gb + 1
+        if r.margin is not None:
+            rep.margin_positions += int(np.sum(r.margin < tol)) + int(r.final_gap < tol)
         if gpu_num[b] < 1:
             rep.failures.append((b, "gpu row error", int(gpu_num[b])))
             continue
@@ -89,4 +111,34 @@ def compare(oracle, gpu_tokens, gpu_num, gpu_alpha, gpu_p, gpu_q, draft_tokens, 
             rep.failures.append((b, "accepted prefix differs from drafts"))
         if int(toks[k]) not in r.outcomes[k]:
             rep.failures.append((b, "final token not admissible", int(toks[k]), r.outcomes[k][:8]))
+    return rep
+
+
+def oracle_threads():
+    """Threads for the oracle: the cores this process may run on."""
+    import os
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def full_batch_parity(w, gpu, rows=None, chunk=64, threads=None, tol=TOL) -> ParityReport:
+    """Every row (or the listed rows) of a workload whose logits are device tensors, compared with
+    the fp64 oracle. Rows come to the host `chunk` at a time from the calling thread; the oracle
+    runs each chunk's rows in a thread pool. gpu: the numpy outputs (tokens, num, alpha, p, q)."""
+    from oracle.spec_verify_oracle import oracle_verify_rows
+    threads = threads or oracle_threads()
+    rows = list(range(w.B)) if rows is None else list(rows)
+    rep = ParityReport()
+    for c0 in range(0, len(rows), chunk):
+        part = rows[c0:c0 + chunk]
+        host = {}
+        for b in part:
+            host[b] = w.host_rows(b)
+        o = oracle_verify_rows(lambda b: host[b], w.draft_tokens, w.draft_len, w.temperature,
+                               w.uniforms, w.G, w.V, part, threads=threads, diagnostics=True,
+                               eps=tol)
+        rep.merge(compare(o, *gpu, w.draft_tokens, w.draft_len, rows=part, tol=tol))
+        del host, o
     return rep

@@ -450,3 +450,30 @@ def test_accept_is_strict_at_the_ratio():
         u = np.array([[u0, 0.25, 0.25]], np.float32)
         r = oracle_verify(zt, zd, np.array([[0]]), np.array([1]), np.ones(1, np.float32), u)
         assert r.out_num_emitted[0] - 1 == k
+
+
+def test_threaded_row_driver_equals_the_batch_oracle():
+    """oracle_verify_rows (rows in a thread pool) gives what oracle_verify gives, row for row."""
+    from oracle.spec_verify_oracle import oracle_verify_rows
+    zt, zd, x, n, T, u = _small_row(G=3, V=40, seed=11)
+    rng = np.random.default_rng(12)
+    B = 9
+    zt = np.concatenate([zt] * B) + rng.normal(0, 1, (B,) + zt.shape[1:])
+    zd = np.concatenate([zd] * B) + rng.normal(0, 1, (B,) + zd.shape[1:])
+    x = np.concatenate([x] * B)
+    n = rng.integers(0, 4, B).astype(np.int32)
+    T = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    T[2] = 0.0
+    u = rng.random((B, 5), dtype=np.float32)
+    ref = oracle_verify(zt, zd, x, n, T, u, diagnostics=True)
+    rows = [0, 2, 3, 5, 8]
+    got = oracle_verify_rows(lambda b: (zt[b], zd[b]), x, n, T, u, 3, 40, rows, threads=3,
+                             diagnostics=True)
+    for b in range(B):
+        if b in rows:
+            assert got.rows[b].tokens == ref.rows[b].tokens and got.rows[b].k == ref.rows[b].k
+            assert np.array_equal(got.out_alpha[b], ref.out_alpha[b])
+            assert got.rows[b].exact == ref.rows[b].exact
+        else:
+            assert got.rows[b] is None and got.out_num_emitted[b] == -1
+    assert np.array_equal(got.out_tokens[rows], ref.out_tokens[rows])
