@@ -36,6 +36,10 @@
  * Asynchrony: calls validate their arguments on the host, enqueue work on `cuda_stream` (NULL = the
  * legacy default stream) and return. Outputs are valid once that stream has been synchronised.
  *
+ * Row limits: rows whose byte length V * s is a multiple of 16, with 16-byte aligned logit bases,
+ * run on the streaming kernel: bf16 V <= 1048576, fp32 V <= 311296. Any other V or alignment runs
+ * on the element kernel: V <= 262144. Larger V returns SV_ERR_BAD_SHAPE.
+ *
  * Errors: argument errors return a nonzero sv_status synchronously and enqueue nothing. Launch
  * errors return SV_ERR_CUDA. Data errors never trap: they mark the row (out_num_emitted[b] = -1,
  * out_tokens[b, :] = -1, out_alpha/p/q[b, :] = 0). Row data errors are: draft_len outside [0, G];
@@ -56,8 +60,8 @@ extern "C" {
 typedef enum {
   SV_OK = 0,
   SV_ERR_NULL_POINTER = 1,        /* a required pointer is NULL                                   */
-  SV_ERR_BAD_SHAPE = 2,           /* B < 1, gamma_max outside [0, SV_MAX_GAMMA], V < 1, V too large
-                                     for one thread-block cluster, or the launch grid overflows    */
+  SV_ERR_BAD_SHAPE = 2,           /* B < 1, gamma_max outside [0, SV_MAX_GAMMA], V < 1, V beyond
+                                     the row limits below, or the launch grid overflows            */
   SV_ERR_BAD_DTYPE = 3,           /* dtype is not an sv_dtype                                     */
   SV_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < spec_verify_workspace_size(...), or NULL   */
   SV_ERR_MISALIGNED = 5,          /* a pointer is not aligned to its element type (workspace: 16 B) */

@@ -35,7 +35,8 @@ namespace {
 #endif
 
 constexpr int kElemThreads = 512;
-constexpr int kVptOptions[4] = {1, 2, 4, 8};
+// Logits per thread of the element kernel: up to 16 CTAs x 512 threads x 32 = 262144 logits a row.
+constexpr int kVptOptions[6] = {1, 2, 4, 8, 16, 32};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -51,7 +52,7 @@ bool sizes_ok(int32_t B, int32_t G, int32_t V, int32_t dtype) {
 
 // Element path: a row of V logits split into C <= 16 chunks of at most 512 * VPT logits.
 bool element_plan(int V, int* vpt_index, int* C, int* per) {
-  for (int vi = 0; vi < 4; ++vi) {
+  for (int vi = 0; vi < 6; ++vi) {
     const long long cap = static_cast<long long>(kElemThreads) * kVptOptions[vi];
     const long long c = (V + cap - 1) / cap;
     if (c <= sv::kMaxCluster) {

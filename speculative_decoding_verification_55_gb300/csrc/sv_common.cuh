@@ -554,6 +554,47 @@ __device__ __forceinline__ bool row_scalars_ok(const Params& P, int b, int gb, b
 }
 
 // ------------------------------------------------------------------------------------------------
+// Positions of the batch
+// ------------------------------------------------------------------------------------------------
+
+struct Pos {
+  int b, i, gb;
+  float T;
+  bool len_ok, t_ok, greedy, load, two, oh;   // two: a draft row is read; oh: one-hot draft
+};
+
+// Slot s in position-major order (s = i * B + b): the slots a cluster strides over mix every
+// position index, so ragged rows (fewer positions at large i) and the cheaper bonus positions
+// spread evenly over the clusters.
+__device__ __forceinline__ Pos classify(const Params& P, int s) {
+  Pos p;
+  p.i = s / P.B;
+  p.b = s - p.i * P.B;
+  if (P.tree) {                       // tree nodes: greedy positions 0 .. size-1 of the row
+    p.gb = (P.tsize ? __ldg(P.tsize + p.b) : P.G + 1) - 1;
+    p.T = 0.0f;
+    p.len_ok = p.gb >= 0 && p.gb <= P.G;
+    p.greedy = p.t_ok = true;
+    p.load = p.len_ok && p.i <= p.gb;
+    p.two = p.oh = false;
+    return p;
+  }
+  p.gb = P.draft_len ? __ldg(P.draft_len + p.b) : P.G;
+  p.T = __ldg(P.temperature + p.b);
+  p.len_ok = p.gb >= 0 && p.gb <= P.G;
+  p.greedy = (p.T == 0.0f);
+  p.t_ok = p.greedy || (p.T >= FLT_MIN && p.T <= FLT_MAX);   // NaN fails both
+  p.load = p.len_ok && p.t_ok && p.i <= p.gb;
+  p.two = p.load && !p.greedy && p.i < p.gb && !P.onehot;
+  p.oh = p.load && !p.greedy && p.i < p.gb && P.onehot;
+  if (P.split && !row_unfiltered(P, p.b)) {   // the filter kernel's row: no work, no error here
+    p.len_ok = p.t_ok = true;
+    p.load = p.two = p.oh = false;
+  }
+  return p;
+}
+
+// ------------------------------------------------------------------------------------------------
 // Finish a position (one full warp of the CTA that holds the position's final result): outputs of
 // the position, its record, its arrival on the row counter and, for the row's last arrival, the
 // row's emit: k = first rejected position (else gamma_b), tokens x_0..x_{k-1} then the correction
@@ -716,6 +757,154 @@ __device__ __forceinline__ bool earlier_rejection(const Params& P, int b, int i,
 }
 
 // ------------------------------------------------------------------------------------------------
+// Draws inside one CTA's chunk
+// ------------------------------------------------------------------------------------------------
+
+// The vector with element e set to -inf (a one-hot draft's token, left out of a sum).
+template <bool BF16>
+__device__ __forceinline__ uint4 mask_elem(uint4 v, int e) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (BF16) {
+      if (e == 2 * q) w[q] = (w[q] & 0xffff0000u) | 0xff80u;
+      if (e == 2 * q + 1) w[q] = (w[q] & 0x0000ffffu) | 0xff800000u;
+    } else if (e == q) {
+      w[q] = 0xff800000u;
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Sum over the G consecutive lanes of a group (vectors u, u+1, ... of a chunk sit in consecutive
+// lanes); every lane of the group gets the total.
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < G; o <<= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// The draw inside this CTA's chunk (kNT consumer threads meeting at named barrier kBarId; `sm`
+// provides scan_wt, scan_slot, widx (one entry per warp), dj, dbefore, dover). usum[g] holds the weight of vectors u0 + g*kGrp ... +kGrp-1
+// (residual or p weights, per `resid`); the token is the first logit whose running weight exceeds
+// t_local, else (rounding) the last logit with positive weight. Block-wide prefix sum over the
+// group sums, then one reload of the crossing group. Returns the token in warp `finisher` (all its
+// lanes); other warps return -1. All consumer threads call it. Token `skip_tok` (if >= 0) has weight 0
+// (the usum entries already leave it out).
+template <bool BF16, int kGrp, int kNT, int kBarId, typename SM>
+__device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, const char* rowt,
+                          const char* rowd, bool resid, float k, float ct, float cd, float cb,
+                          SM& sm, int ctid, int& finisher, int skip_tok = -1) {
+  constexpr int kCT = kNT, kCW = kNT / 32;
+  constexpr int E = BF16 ? 8 : 4;
+  const int lane = ctid & 31, cw = ctid >> 5;
+  const int cg = (cu + kGrp - 1) / kGrp;
+  const int run = (cg + kCT - 1) / kCT;
+  const int r0 = min(ctid * run, cg), r1 = min(r0 + run, cg);
+  float tsum = 0.0f;
+  int last_j = -1;
+  for (int j = r0; j < r1; ++j) {
+    const float v = usum[j];
+    tsum += v;
+    if (v > 0.0f) last_j = j;
+  }
+  const float incl = warp_incl_scan(tsum, lane);
+  float excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.0f;
+  if (lane == 31) sm.scan_wt[cw] = incl;
+  int lj = last_j;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lj = max(lj, __shfl_xor_sync(kFull, lj, o));
+  if (lane == 0) sm.widx[cw] = lj;
+  named_bar_sync(kBarId, kCT);
+  float wexcl = 0.0f;
+#pragma unroll
+  for (int w2 = 0; w2 < kCW; ++w2)
+    if (w2 < cw) wexcl += sm.scan_wt[w2];
+  const bool cross = (tsum > 0.0f) && (wexcl + incl > t_local);
+  const unsigned m = __ballot_sync(kFull, cross);
+  if (lane == 0) sm.scan_slot[cw] = m ? (cw * 32 + __ffs(m) - 1) : INT_MAX;
+  named_bar_sync(kBarId, kCT);
+  int win = INT_MAX, best_j = -1;
+#pragma unroll
+  for (int w2 = 0; w2 < kCW; ++w2) {
+    win = min(win, sm.scan_slot[w2]);
+    best_j = max(best_j, sm.widx[w2]);
+  }
+  // The crossing vector and the weight before it (winner thread), else the last positive vector.
+  if (win != INT_MAX && ctid == win) {
+    float c = wexcl + excl;
+    int lastpos = -1, vj = -1;
+    float c_last = c, before = 0.0f;
+    for (int j = r0; j < r1; ++j) {
+      const float v = usum[j];
+      if (v > 0.0f) {
+        if (c + v > t_local) {
+          vj = j;
+          before = c;
+          break;
+        }
+        lastpos = j;
+        c_last = c;
+        c += v;
+      }
+    }
+    const bool over = vj < 0;        // rounding: the run's sums crossed, its vectors did not
+    sm.dj = over ? lastpos : vj;
+    sm.dbefore = over ? c_last : before;
+    sm.dover = over;
+  } else if (win == INT_MAX && ctid == 0) {
+    sm.dj = best_j;
+    sm.dbefore = 0.0f;
+    sm.dover = 1;
+  }
+  named_bar_sync(kBarId, kCT);   // after this no thread reads usum: the caller may reuse it
+  finisher = (win == INT_MAX) ? 0 : (win >> 5);
+  if (cw != finisher) return -1;
+  const int vj = sm.dj;
+  const float before = sm.dbefore;
+  const bool overrun = sm.dover != 0;
+  int tok = -1;
+  if (lane == 0 && vj >= 0) {
+    // Scan the group's vectors in index order: the first logit whose running weight exceeds the
+    // threshold, else the last positive one.
+    const f32x2 k2 = pk(k, k), c2 = pk(ct, cd);
+    const int ga = u0 + vj * kGrp, gz = min(ga + kGrp, u0 + cu);
+    float c = before;
+    int pick = -1, lastp = -1;
+    for (int u = ga; u < gz && (pick < 0 || overrun); ++u) {
+      uint4 t = ld_stream_v4(reinterpret_cast<const uint4*>(rowt) + u);
+      if (skip_tok >= 0 && u == skip_tok / E) t = mask_elem<BF16>(t, skip_tok - u * E);   // weight 0
+      const uint4 d = resid ? ld_stream_v4(reinterpret_cast<const uint4*>(rowd) + u) : t;
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        float w0, w1;
+        if (resid) {
+          resid_pair<BF16>(t, d, e, k2, c2, w0, w1);
+        } else {
+          w0 = ex2(fmaf(vec_get<BF16>(t, e), k, cb));
+          w1 = ex2(fmaf(vec_get<BF16>(t, e + 1), k, cb));
+        }
+        if (w0 > 0.0f) {
+          lastp = u * E + e;
+          c += w0;
+          if (pick < 0 && c > t_local) pick = u * E + e;
+        }
+        if (w1 > 0.0f) {
+          lastp = u * E + e + 1;
+          c += w1;
+          if (pick < 0 && c > t_local) pick = u * E + e + 1;
+        }
+      }
+    }
+    if (pick < 0 || overrun) pick = lastp;
+    tok = pick;
+  }
+  return __shfl_sync(kFull, tok, 0);
+}
+
+// ------------------------------------------------------------------------------------------------
 // Host-side launchers (defined in the kernel translation units)
 // ------------------------------------------------------------------------------------------------
 
@@ -727,7 +916,7 @@ int verify_args_status(const void* target_logits, const void* draft_logits,
                        int32_t* out_num_emitted, float* out_alpha, float* out_p_draft,
                        float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
 
-// Element path (any alignment, V <= 16 * 512 * 8): one cluster per position slot.
+// Element path (any alignment, V <= 16 * 512 * 32): one cluster per position slot.
 cudaError_t launch_element(const Params& P, bool bf16, int vpt_index, cudaStream_t stream);
 // Streaming path (16-byte aligned rows): persistent clusters fed by bulk copies.
 cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream);

@@ -451,7 +451,9 @@ KernelFn element_kernel(int vpt_index) {
     case 0: return sv_element_kernel<BF16, 1>;
     case 1: return sv_element_kernel<BF16, 2>;
     case 2: return sv_element_kernel<BF16, 4>;
-    default: return sv_element_kernel<BF16, 8>;
+    case 3: return sv_element_kernel<BF16, 8>;
+    case 4: return sv_element_kernel<BF16, 16>;
+    default: return sv_element_kernel<BF16, 32>;
   }
 }
 

@@ -90,9 +90,11 @@ def test_argument_errors_are_host_side(L):
     assert call(L, ws=None) == 4                      # SV_ERR_WORKSPACE_TOO_SMALL
     assert call(L, wsb=16) == 4
     # Rows whose byte length is not a multiple of 16 take the element path, which holds at most
-    # 16 * 512 * 8 logits per row (16-byte rows stream and have no such limit).
-    assert call(L, V=65537) == 2
-    assert call(L, dtype=0, V=65539) == 2
+    # 16 * 512 * 32 logits per row; 16-byte rows stream, up to 1048576 bf16 or 311296 fp32 logits.
+    assert call(L, V=262145) == 2
+    assert call(L, dtype=0, V=262147) == 2
+    assert call(L, V=1048576 + 8) == 2
+    assert call(L, dtype=0, V=311296 + 4) == 2
 
 
 def call_filtered(L, **kw):

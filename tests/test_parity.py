@@ -27,6 +27,11 @@ def run_gpu(sv, tensors):
                     tensors["draft_len"], tensors["temperature"], tensors["uniforms"],
                     with_probs=True)
     torch.cuda.synchronize()
+    zt = tensors["target_logits"]
+    B, G1, V = zt.shape
+    dcode = sv.SV_DTYPE_BF16 if zt.dtype == torch.bfloat16 else sv.SV_DTYPE_F32
+    ws = sv.workspace_for(B, G1 - 1, V, dcode, zt.device)
+    assert sv.spec_verify_workspace_status(ws, B, G1 - 1) == 0, "a bounded wait gave up"
     return [o.cpu().numpy() for o in out]
 
 
@@ -130,6 +135,31 @@ def test_edge_draft_widths(sv, G):
     gpu = run_gpu(sv, to_dev(*args, "bf16"))
     o = oracle_verify(*args, diagnostics=True)
     check(o, gpu, args[2], args[3])
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 100277), ("f32", 151937), ("bf16", 262143)])
+def test_unaligned_large_vocabularies(sv, dtype, V):
+    """Rows whose byte length is not a multiple of 16 above 65536 logits: the element kernel with 16
+    or 32 logits per thread, ragged lengths and a greedy mix, against the oracle."""
+    B, G = 6, 3
+    args = small_inputs(B, G, V, dtype, seed=V % 1000, greedy_frac=0.3)
+    gpu = run_gpu(sv, to_dev(*args, dtype))
+    rep = check(oracle_verify(*args, diagnostics=True), gpu, args[2], args[3])
+    print(f"{dtype} V={V}: {rep}")
+
+
+def test_vocabulary_beyond_the_row_limits_is_rejected(sv):
+    """V above the element kernel's 262144 logits (rows not of 16-byte multiples) returns
+    SV_ERR_BAD_SHAPE before anything is enqueued."""
+    B, G, V = 1, 1, 262145
+    dev = torch.device("cuda")
+    zt = torch.zeros((B, G + 1, V), dtype=torch.float32, device=dev)
+    zd = torch.zeros((B, G, V), dtype=torch.float32, device=dev)
+    with pytest.raises(sv.SpecVerifyError) as ei:
+        sv.verify(zt, zd, torch.zeros((B, G), dtype=torch.int32, device=dev), None,
+                  torch.ones((B,), dtype=torch.float32, device=dev),
+                  torch.full((B, G + 2), 0.5, dtype=torch.float32, device=dev))
+    assert ei.value.status == 2
 
 
 def test_scalar_path_large_vocab_and_misaligned_base(sv):
