@@ -282,7 +282,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 // Bounded waits: every spin gives up after kSpinLimit polls (each poll may suspend the thread for a
 // hardware-chosen time), so a broken protocol ends the kernel with an error status instead of a hang.
-constexpr int kSpinLimit = 1 << 22;
+// A CTA that waits for its own bulk copies to land before it exits (they always land: they read
+// valid memory) allows kDrainLimit polls.
+#ifndef SV_SPIN_LIMIT
+#define SV_SPIN_LIMIT (1 << 22)
+#endif
+constexpr int kSpinLimit = SV_SPIN_LIMIT;
+constexpr int kDrainLimit = 1 << 26;
+
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  for (int n = 0; n < kDrainLimit; ++n)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (int n = 0; n < kSpinLimit; ++n)

@@ -1331,8 +1331,8 @@ __global__ void __launch_bounds__(kFT, 1) sv_filter_kernel(const Params P) {
   // A copy that timed out, or one issued ahead for a position the cluster did not reach, may still
   // land: wait for it (bounded) before this CTA can exit.
   if (tid == 0) {
-    if (my_tmo) mbar_wait(smem_addr(&sm.bar), (npos - 1) & 1);
-    if (pf >= 0) mbar_wait(smem_addr(&sm.bar), npos & 1);
+    if (my_tmo) mbar_wait_drain(smem_addr(&sm.bar), (npos - 1) & 1);
+    if (pf >= 0) mbar_wait_drain(smem_addr(&sm.bar), npos & 1);
   }
   cluster_sync_all();        // no CTA leaves while a peer may still read its shared memory
 }

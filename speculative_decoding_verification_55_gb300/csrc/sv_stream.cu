@@ -39,7 +39,11 @@
 //            picks the token inside it. A bonus draw first fills the group sums of p from L2.
 //   finish   the CTA holding the position's final result writes it; the row's last position to
 //            finish writes the row's outputs (an arrival counter per row, no waiting).
-// Every wait is bounded; a wait that gives up sets the status word and ends the kernel.
+// Every wait is bounded; a wait that gives up sets the status word, marks the rows the CTA was
+// working on as errors and ends the CTA's work. The CTAs of a cluster leave together, at a hardware
+// cluster barrier that every thread reaches (all waits before it are bounded), so none leaves while
+// a peer may still push into its shared memory, and a producer that stopped first lets its own
+// in-flight copies land.
 //
 // The operation: [R] "Speculative decoding", rayaq.ca ml-models -- Mechanics, One round, steps 3-5;
 // Why the output is exactly the target's; The greedy case; Implementation. [B]
@@ -108,6 +112,11 @@ constexpr int kMaxGroupsOf = (stream_max_units(BF16, G == kGrpWide) + G - 1) / G
 template <bool BF16, int G>
 constexpr int kDynBytesOf = kSlotBytes * kSlotsOf<BF16> + kMaxGroupsOf<BF16, G> * 4;
 constexpr int kConsumerBar = 1;               // named barrier of the consumer warps
+#ifndef SV_STREAM_STOP_POLL
+#define SV_STREAM_STOP_POLL 64
+#endif
+constexpr int kStopPoll = SV_STREAM_STOP_POLL;   // producer polls between looks at the stop flag
+static_assert((kStopPoll & (kStopPoll - 1)) == 0, "a power of two");
 
 enum : unsigned { kStatusTimeout = 1u };
 
@@ -115,7 +124,6 @@ struct Shared {
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
   uint64_t xbar[2];                  // exchange: bytes pushed by every CTA complete it, by parity
-  uint64_t xdone;                    // end-of-kernel arrivals
   float4 xrec[2][kMaxCluster];       // per rank: (m_p, s_p, m_q, s_q), or (argmax value, index)
   uint2 xaux[2][kMaxCluster];        // per rank: (bad flag, residual total of the pending position)
   float4 wpart[kCW];                 // warp partials
@@ -184,7 +192,6 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       mbar_init(smem_addr(&sm.empty[s]), kCW);
     }
     for (int s = 0; s < 2; ++s) mbar_init(smem_addr(&sm.xbar[s]), 1);
-    mbar_init(smem_addr(&sm.xdone), C);
     sm.stop = 0;
     sm.stop_snap = 0;
     fence_mbarrier_init_cluster();
@@ -194,11 +201,23 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
   const uint32_t ring_addr = smem_addr(dyn);
 
   // ------------------------------------------------------------------ producer
+  // The whole warp walks the loop in step (so it never diverges and reaches the final cluster
+  // barrier together); lane 0 alone arms the barriers and issues the copies.
   if (warp == kCW) {
-    if (lane != 0) return;
     uint32_t tc = 0;
     bool ok = true;
     const uint64_t keep = l2_policy_evict_last(), once = l2_policy_evict_first();
+    // A free ring slot; gives up when the consumers stopped (looked at every kStopPoll polls) or
+    // after the spin limit. Warp-uniform.
+    auto acquire = [&](uint32_t slot, uint32_t par) -> bool {
+      for (int n = 0; n < kSpinLimit; ++n) {
+        if (__all_sync(kFull, mbar_try_wait(smem_addr(&sm.empty[slot]), par))) return true;
+        if ((n & (kStopPoll - 1)) == kStopPoll - 1 &&
+            __any_sync(kFull, *reinterpret_cast<volatile int*>(&sm.stop) != 0))
+          return false;
+      }
+      return false;
+    };
     for (int s = cid; s < total && ok; s += P.nclusters) {
       const Pos p = classify(P, s);
       if (!p.load) continue;
@@ -209,15 +228,17 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         g += static_cast<size_t>(u0) * 16;
         for (int ks = 0; ks < nsl; ++ks, ++tc) {
           const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
-          if (!mbar_wait(smem_addr(&sm.empty[slot]), par ^ 1) || sm.stop) {
+          if (!acquire(slot, par ^ 1)) {
             ok = false;
             break;
           }
           const uint32_t bytes = static_cast<uint32_t>(min(kSlotUnits, cu - ks * kSlotUnits)) * 16;
-          mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), bytes);
-          // A drafted position's chunks are read again by the residual pass: keep them in L2.
-          bulk_g2s(ring_addr + slot * kSlotBytes, g + static_cast<size_t>(ks) * kSlotBytes, bytes,
-                   smem_addr(&sm.full[slot]), p.two ? keep : once);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), bytes);
+            // A drafted position's chunks are read again by the residual pass: keep them in L2.
+            bulk_g2s(ring_addr + slot * kSlotBytes, g + static_cast<size_t>(ks) * kSlotBytes, bytes,
+                     smem_addr(&sm.full[slot]), p.two ? keep : once);
+          }
         }
       }
       if (!p.two || !ok) continue;
@@ -229,27 +250,28 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       const char* gd = static_cast<const char*>(P.zd) + ((size_t)p.b * G + p.i) * Vs * ES + (size_t)u0 * 16;
       for (int ks = 0; ks < nsl2; ++ks, ++tc) {
         const uint32_t slot = tc % kNumSlots, par = (tc / kNumSlots) & 1;
-        if (!mbar_wait(smem_addr(&sm.empty[slot]), par ^ 1) || sm.stop) {
+        if (!acquire(slot, par ^ 1)) {
           ok = false;
           break;
         }
         const int blk = nsl2 - 1 - ks;
         const uint32_t bytes = static_cast<uint32_t>(min(kHalfUnits, cu - blk * kHalfUnits)) * 16;
         const size_t off = static_cast<size_t>(blk) * kHalfUnits * 16;
-        mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), 2 * bytes);
-        bulk_g2s(ring_addr + slot * kSlotBytes, gt + off, bytes, smem_addr(&sm.full[slot]), once);
-        bulk_g2s(ring_addr + slot * kSlotBytes + kSlotBytes / 2, gd + off, bytes,
-                 smem_addr(&sm.full[slot]), once);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(smem_addr(&sm.full[slot]), 2 * bytes);
+          bulk_g2s(ring_addr + slot * kSlotBytes, gt + off, bytes, smem_addr(&sm.full[slot]), once);
+          bulk_g2s(ring_addr + slot * kSlotBytes + kSlotBytes / 2, gd + off, bytes,
+                   smem_addr(&sm.full[slot]), once);
+        }
       }
     }
-    if (!ok) {
-      set_status(P, sm, kStatusTimeout);
-      // Let the copies already issued land before this CTA can exit.
-      for (uint32_t t = tc > kNumSlots ? tc - kNumSlots : 0; t < tc; ++t)
-        mbar_wait(smem_addr(&sm.full[t % kNumSlots]), (t / kNumSlots) & 1);
-    }
-    return;
-  }
+    if (!ok && lane == 0) set_status(P, sm, kStatusTimeout);
+    // Let the copies already issued land before this CTA can exit (the consumers may have stopped
+    // before reading them; when they read every slot, these phases are complete already).
+    for (uint32_t t = tc > kNumSlots ? tc - kNumSlots : 0; t < tc; ++t)
+      mbar_wait_drain(smem_addr(&sm.full[t % kNumSlots]), (t / kNumSlots) & 1);
+    __syncwarp();
+  } else {
 
   // ------------------------------------------------------------------ consumers
   const int ctid = tid;          // 0 .. kCT-1
@@ -326,7 +348,12 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         }
         rbad = __any_sync(kFull, lane < kCW && sm.wbad[lane]);
       }
+#ifdef SV_TEST_DROP_RANK0_PUSHES
+      // Test builds only: rank 0 pushes nothing, so every exchange wait of the cluster runs out.
+      if (lane < C && rank != 0) {
+#else
       if (lane < C) {
+#endif
         const uint32_t bar_r = map_to_rank(smem_addr(&sm.xbar[par]), lane);
         st_async_v4(map_to_rank(smem_addr(&sm.xrec[par][rank]), lane), __float_as_uint(rec.x),
                     __float_as_uint(rec.y), __float_as_uint(rec.z), __float_as_uint(rec.w), bar_r);
@@ -612,7 +639,16 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
 
     // ---- the cluster exchange: this position's softmax partials + the pending residual totals ----
     exchange(true, kind, p, x, k, zx_t, zx_d, u_acc, u_res, u_bon);
-    if (sm.stop_snap) break;
+    if (sm.stop_snap) {
+      // A wait gave up: this position (and the pending one) will never finish, so their rows
+      // would never be written. Mark them as errors; the status word tells the caller why.
+      if (cw == 0) {
+        if (P.tree) write_tree_row_error(P, p.b, lane);
+        else write_row_error(P, p.b, lane);
+        if (pv && !P.tree) write_row_error(P, sm.pend.b, lane);
+      }
+      break;
+    }
     finish_pending();
     // The CTA that finishes this position when no draw picks one: rotates over the ranks so that
     // the finishing work (records, counters, row emits) does not slow one rank down.
@@ -756,14 +792,17 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
   if (pv && !sm.stop_snap) {
     named_bar_sync(kConsumerBar, kCT);   // the last residual partials are in place
     exchange(false, kVerify, Pos{}, -1, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
-    finish_pending();
+    if (!sm.stop_snap) {
+      finish_pending();
+    } else if (cw == 0 && !P.tree) {     // the pending position will never finish
+      write_row_error(P, sm.pend.b, lane);
+    }
+  }
+
   }
 
   // ---- no CTA leaves while a peer may still write into its shared memory ----
-  if (cw == 0) {
-    if (lane < C) mbar_arrive_remote(map_to_rank(smem_addr(&sm.xdone), lane));
-    if (!mbar_wait_cluster(smem_addr(&sm.xdone), 0)) set_status(P, sm, kStatusTimeout);
-  }
+  cluster_sync_all();
 }
 
 // bf16 one-hot launches take the wide draw groups; the rest the narrow ones.
