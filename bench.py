@@ -595,14 +595,14 @@ def run_gpu(args):
                        "padded_positions_per_gpu": B * (G + 1),
                        "algorithmic_bytes_per_step": algo_bytes,
                        "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
-            # --filter: the streaming kernel takes the unfiltered and greedy rows, then the filter
-            # kernel the rest (two launches a step; the step's time is the roofline's)
+            # --filter: the threshold kernel, then the masked streaming kernel (two launches a
+            # step; the step's time is the roofline's)
             "gpu_launches": args.steps * (2 if args.filter else 1),
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                          "frac": achieved_gbs / peak, "peak_kind": peak_kind,
                          "frac_of_8tbs": achieved_gbs / NOMINAL_HBM_GBS, "traffic": traffic,
-                         "kernel": ("sv_filter_kernel" if args.filter else "sv_stream_kernel")
-                         + ("<bf16>" if cfg.dtype == "bf16" else "<f32>")},
+                         "kernel": ("sv_threshold_kernel + masked " if args.filter else "")
+                         + "sv_stream_kernel" + ("<bf16>" if cfg.dtype == "bf16" else "<f32>")},
             "clocks": clock_info,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -78,12 +78,16 @@ typedef enum { SV_DTYPE_F32 = 0, SV_DTYPE_BF16 = 1 } sv_dtype;
 /* Size of the library's static device scratch used by spec_verify_noalloc (1 MiB per device). */
 #define SV_NOALLOC_SCRATCH_BYTES (1u << 20)
 
-/* Bytes of device workspace spec_verify needs for these sizes (per-position records, one arrival
- * counter per row and a status word), a multiple of 256. Returns 0 for invalid sizes.
+/* Bytes of device workspace the verification calls need for these sizes (per-position records, one
+ * arrival counter per row, a status word, then B * (2 * gamma_max + 1) fp32 row thresholds and a
+ * row counter that only spec_verify_filtered uses), a multiple of 256. Returns 0 for invalid sizes.
+ * The thresholds and the counter fill the last round_up(4 * (B * (2 * gamma_max + 1) + 1), 256)
+ * bytes.
  *
  * The workspace must hold zeros before its first use (e.g. one cudaMemset after allocation). Every
- * call that runs to completion leaves it zeroed again, so it can be reused without clearing. One
- * workspace serves one call at a time: two calls in flight on the same workspace race. */
+ * call that runs to completion leaves it zeroed again, so it can be reused without clearing, also
+ * by calls of other sizes. One workspace serves one call at a time: two calls in flight on the same
+ * workspace race. */
 size_t spec_verify_workspace_size(int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
 
 /* Batched verification of one speculative round ([R] One round, steps 3-5; [R] The greedy case).
@@ -187,20 +191,23 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
  *         together; the largest logit is always kept);
  *   renormalise the kept probabilities.
  * Then the rule of spec_verify on the filtered p~, q~: keep x_i while u[b,i] < min(1, p~(x)/q~(x))
- * (q~(x) = 0 reads as 1); at the first rejection draw from max(0, p~ - q~) (from p~ when that has
- * no mass) with u[b,G]; after gamma_b accepts draw the bonus from the filtered target p~ with
- * u[b,G+1]; alpha_i = sum_v min(p~, q~); out_p_draft / out_q_draft are p~(x) and q~(x).
+ * (where q~(x) = 0 the ratio is 1 if p~(x) > 0, else 0); at the first rejection draw from
+ * max(0, p~ - q~) (from p~ when that has no mass) with u[b,G]; after gamma_b accepts draw the bonus
+ * from the filtered target p~ with u[b,G+1]; alpha_i = sum_v min(p~, q~); out_p_draft /
+ * out_q_draft are p~(x) and q~(x).
  * Greedy rows are verified as in spec_verify (filtering keeps the argmax).
  *
  * top_k  [B] int32  per-row k; <= 0 or >= V turns top-k off. NULL: off for every row.
  * top_p  [B] fp32   per-row nucleus mass; >= 1 turns top-p off; a sampled row with top_p NaN or
  *                   <= 0 is a row error (outputs -1 / 0). NULL: off for every row.
- * The call enqueues two kernels on `cuda_stream`: the streaming kernel of spec_verify_ex for the
- * rows whose filters are off and the greedy rows, then the filter kernel for the other rows.
+ * Both filters keep an upper set of the row's logits, so one threshold per row describes them: the
+ * call enqueues on `cuda_stream` the threshold kernel of spec_verify_filter_thresholds (into the
+ * workspace), the streaming kernel of spec_verify_ex reading every logit below its row's threshold
+ * as -inf, and a memset that clears the thresholds again.
  * Everything else (arguments, layout, ownership, workspace, errors) as in spec_verify_ex. Only rows
  * of 16-byte multiples are supported (else SV_ERR_BAD_SHAPE), with 16-byte aligned logit bases
- * (else SV_ERR_MISALIGNED), and V at most 16 * 65536 bytes of logits per row (bf16 V <= 524288,
- * fp32 V <= 262144; else SV_ERR_BAD_SHAPE). */
+ * (else SV_ERR_MISALIGNED), within the streaming kernel's row limits (bf16 V <= 1048576, fp32
+ * V <= 311296; else SV_ERR_BAD_SHAPE). */
 int spec_verify_filtered(const void* target_logits, const void* draft_logits,
                          const int32_t* draft_tokens, const int32_t* draft_len,
                          const float* temperature, const int32_t* top_k, const float* top_p,
@@ -208,6 +215,28 @@ int spec_verify_filtered(const void* target_logits, const void* draft_logits,
                          float* out_alpha, float* out_p_draft, float* out_q_draft,
                          int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                          void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* The per-row thresholds of top-k / top-p filtering that spec_verify_filtered applies: for every
+ * logit row the rule reads in a sampled batch row whose top_k or top_p is on, the smallest logit
+ * the filters keep (defined as in spec_verify_filtered: the kept set is exactly the logits >= the
+ * threshold); -inf for every other row (greedy rows, rows not read, rows whose filters are off, and
+ * rows spec_verify_filtered reports as row errors: a bad draft_len, temperature or top_p, or a
+ * logit row holding NaN or +inf, or only -inf). [R] "Speculative decoding", rayaq.ca ml-models --
+ * Why the output is exactly the target's.
+ *
+ * target_logits, draft_logits, draft_len, temperature, top_k, top_p, B, gamma_max, V, dtype
+ *                  as in spec_verify_filtered (device pointers; draft_len may be NULL).
+ * out_thresholds   [B * (2 * gamma_max + 1)] fp32, device: target rows (b, i), i = 0..G, at
+ *                  b * (G + 1) + i, then draft rows (b, i), i = 0..G-1, at B * (G + 1) + b * G + i.
+ * One CTA per row at a time (a persistent grid), one launch on cuda_stream; nothing else is
+ * written. Errors as in spec_verify_filtered (argument errors enqueue nothing). A top-p decision
+ * within about 1e-6 of the nucleus boundary is taken with fp32 exponentials and 42-bit fixed-point
+ * masses, not in exact arithmetic. */
+int spec_verify_filter_thresholds(const void* target_logits, const void* draft_logits,
+                                  const int32_t* draft_len, const float* temperature,
+                                  const int32_t* top_k, const float* top_p, float* out_thresholds,
+                                  int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                                  void* cuda_stream);
 
 /* KV-cache rollback after a verified round, batched over ragged rows. [R] "Speculative decoding",
  * rayaq.ca ml-models -- Verification attention and the cache: the target's cache held n entries

@@ -25,7 +25,8 @@ SV_ERR_SCRATCH_TOO_SMALL = 8
 SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_onehot",
-            "spec_verify_filtered", "spec_verify_tree_greedy", "spec_verify_kv_rollback",
+            "spec_verify_filtered", "spec_verify_filter_thresholds", "spec_verify_tree_greedy",
+            "spec_verify_kv_rollback",
             "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
             "spec_verify_version")
 
@@ -64,6 +65,9 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_filtered.argtypes = [vp, vp, i32p, i32p, f32p, i32p, f32p, f32p, i32p, i32p,
                                                f32p, f32p, f32p] + tail
             L.spec_verify_filtered.restype = ctypes.c_int
+            L.spec_verify_filter_thresholds.argtypes = [vp, vp, i32p, f32p, i32p, f32p, f32p, i32, i32,
+                                                        i32, i32, vp]
+            L.spec_verify_filter_thresholds.restype = ctypes.c_int
             L.spec_verify_tree_greedy.argtypes = [vp, i32p, i32p, i32p, i32p, i32p, i32p, i32p] + tail
             L.spec_verify_tree_greedy.restype = ctypes.c_int
             L.spec_verify_kv_rollback.argtypes = [i32p, i32p, i32p, i32p, i32p, i32p, vp, ctypes.c_int64,
@@ -373,6 +377,31 @@ def spec_verify_filtered(target_logits, draft_logits, draft_tokens, draft_len, t
             _stream_handle(stream, dev))
     if st != SV_OK:
         raise SpecVerifyError(st, "spec_verify_filtered")
+
+
+def spec_verify_filter_thresholds(target_logits, draft_logits, draft_len, temperature, top_k, top_p,
+                                  out_thresholds, stream=None) -> None:
+    """Calls the C ABI spec_verify_filter_thresholds: per logit row the smallest logit top-k /
+    top-p keep (-inf where nothing is filtered) into out_thresholds [B * (2G + 1)] float32.
+    Raises SpecVerifyError on a nonzero status."""
+    import torch
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    dev = target_logits.device
+    _check(target_logits, "target_logits", device=dev)
+    _check(draft_logits, "draft_logits", dtype=target_logits.dtype, shape=(B, G, V), device=dev)
+    _check(draft_len, "draft_len", torch.int32, (B,), dev)
+    _check(temperature, "temperature", torch.float32, (B,), dev)
+    _check(top_k, "top_k", torch.int32, (B,), dev)
+    _check(top_p, "top_p", torch.float32, (B,), dev)
+    _check(out_thresholds, "out_thresholds", torch.float32, (B * (2 * G + 1),), dev)
+    with _on(dev):
+        st = lib().spec_verify_filter_thresholds(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_len), _ptr(temperature),
+            _ptr(top_k), _ptr(top_p), _ptr(out_thresholds), B, G, V, _dtype_code(target_logits),
+            _stream_handle(stream, dev))
+    if st != SV_OK:
+        raise SpecVerifyError(st, "spec_verify_filter_thresholds")
 
 
 def spec_verify_tree_greedy(target_logits, tree_tokens, tree_parents, tree_size, out_path,

@@ -44,6 +44,14 @@ size_t records_bytes(int32_t B, int32_t G) {
   return align_up(static_cast<size_t>(B) * (G + 1) * sizeof(int2), 256);
 }
 
+// Workspace: records [B, G+1] int2, row counters [B], the status word, then (filtered
+// verification) the row thresholds [B * (2G + 1)] fp32 and the threshold kernel's row counter,
+// which the call clears again after use.
+size_t thresholds_offset(int32_t B, int32_t G) {
+  return align_up(records_bytes(B, G) + static_cast<size_t>(B) * sizeof(unsigned) + 4, 256);
+}
+size_t threshold_rows_of(int32_t B, int32_t G) { return static_cast<size_t>(B) * (2 * G + 1); }
+
 bool sizes_ok(int32_t B, int32_t G, int32_t V, int32_t dtype) {
   if (B < 1 || G < 0 || G > SV_MAX_GAMMA || V < 1) return false;
   if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return false;
@@ -82,8 +90,8 @@ int stream_cluster_size(long long row_bytes, bool bf16,
 
 std::mutex g_mu;
 int g_device_ok[64];                 // 0 unknown, 1 sm_103, 2 other
-int g_max_clusters[64][2][2][5];     // by device, bf16, wide draw groups, log2(C); 0 = not queried
-int g_filter_clusters[64][2][5];     // the same for the filter kernel
+int g_max_clusters[64][2][3][5];     // by device, bf16, variant (narrow, wide, masked), log2(C);
+                                     // 0 = not queried
 
 int check_device(int* dev_out) {
   int dev = 0;
@@ -101,17 +109,16 @@ int check_device(int* dev_out) {
   return g_device_ok[dev] == 1 ? SV_OK : SV_ERR_UNSUPPORTED_DEVICE;
 }
 
-int max_clusters(int dev, bool bf16, int C, int* n, bool filter = false, bool wide = false) {
+// masked: the instantiation of filtered verification (narrow draw groups).
+int max_clusters(int dev, bool bf16, int C, int* n, bool masked = false, bool wide = false) {
   int lg = 0;
   while ((1 << lg) < C) ++lg;
   std::lock_guard<std::mutex> lock(g_mu);
-  wide = wide && bf16 && !filter;
-  int& slot = filter ? g_filter_clusters[dev][bf16 ? 1 : 0][lg]
-                     : g_max_clusters[dev][bf16 ? 1 : 0][wide ? 1 : 0][lg];
+  wide = wide && bf16 && !masked;
+  int& slot = g_max_clusters[dev][bf16 ? 1 : 0][masked ? 2 : (wide ? 1 : 0)][lg];
   if (slot == 0) {
     int m = 0;
-    const cudaError_t e =
-        filter ? sv::filter_max_clusters(bf16, C, &m) : sv::stream_max_clusters(bf16, wide, C, &m);
+    const cudaError_t e = sv::stream_max_clusters(bf16, wide, C, &m, masked);
     if (e != cudaSuccess || m < 1) return SV_ERR_CUDA;
     slot = m;
   }
@@ -152,7 +159,8 @@ extern "C" {
 
 size_t spec_verify_workspace_size(int32_t B, int32_t gamma_max, int32_t V, int32_t dtype) {
   if (!sizes_ok(B, gamma_max, V, dtype)) return 0;
-  return align_up(records_bytes(B, gamma_max) + static_cast<size_t>(B) * sizeof(unsigned) + 4, 256);
+  return thresholds_offset(B, gamma_max) +
+         align_up((threshold_rows_of(B, gamma_max) + 1) * sizeof(float), 256);
 }
 
 const char* spec_verify_status_string(int status) {
@@ -375,6 +383,63 @@ int spec_verify_onehot(const void* target_logits, const int32_t* draft_tokens,
                      V, dtype, workspace, workspace_bytes, cuda_stream, true);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The checks both filtered entry points make before anything is enqueued (the logits' rows: 16-byte
+// multiples on 16-byte aligned bases, within the streaming kernel's row limits).
+int filter_args_status(const void* target_logits, const void* draft_logits, const void* const* ptrs4,
+                       int nptrs, int32_t B, int32_t G, int32_t V, int32_t dtype, int* sC) {
+  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
+  if (!sizes_ok(B, G, V, dtype)) return SV_ERR_BAD_SHAPE;
+  const bool bf16 = dtype == SV_DTYPE_BF16;
+  const uintptr_t es = bf16 ? 2 : 4;
+  auto mis = [](const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; };
+  for (int k = 0; k < nptrs; ++k)
+    if (mis(ptrs4[k], 4)) return SV_ERR_MISALIGNED;
+  if ((static_cast<size_t>(V) * es) % 16 != 0) return SV_ERR_BAD_SHAPE;
+  if (mis(target_logits, 16) || mis(draft_logits, 16)) return SV_ERR_MISALIGNED;
+  if (static_cast<long long>(B) * (2 * G + 1) > INT_MAX / sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
+  *sC = stream_cluster_size(static_cast<long long>(V) * static_cast<long long>(es), bf16);
+  return *sC == 0 ? SV_ERR_BAD_SHAPE : SV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_filter_thresholds(const void* target_logits, const void* draft_logits,
+                                  const int32_t* draft_len, const float* temperature,
+                                  const int32_t* top_k, const float* top_p, float* out_thresholds,
+                                  int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                                  void* cuda_stream) {
+  const int G = gamma_max;
+  if (!target_logits || !temperature || !out_thresholds) return SV_ERR_NULL_POINTER;
+  if (G > 0 && !draft_logits) return SV_ERR_NULL_POINTER;
+  const void* p4[] = {draft_len, temperature, top_k, top_p, out_thresholds};
+  int sC = 0;
+  const int st = filter_args_status(target_logits, draft_logits, p4, 5, B, G, V, dtype, &sC);
+  if (st != SV_OK) return st;
+  int dev = 0;
+  const int dev_status = check_device(&dev);
+  if (dev_status != SV_OK) return dev_status;
+  sv::Params P{};
+  P.zt = target_logits;
+  P.zd = draft_logits;
+  P.draft_len = draft_len;
+  P.temperature = temperature;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.B = B;
+  P.G = G;
+  P.V = V;
+  if (sv::launch_threshold(P, dtype == SV_DTYPE_BF16, out_thresholds, nullptr,
+                           static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 int spec_verify_filtered(const void* target_logits, const void* draft_logits,
                          const int32_t* draft_tokens, const int32_t* draft_len,
                          const float* temperature, const int32_t* top_k, const float* top_p,
@@ -382,35 +447,26 @@ int spec_verify_filtered(const void* target_logits, const void* draft_logits,
                          float* out_alpha, float* out_p_draft, float* out_q_draft,
                          int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                          void* workspace, size_t workspace_bytes, void* cuda_stream) {
-  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
-  if (!sizes_ok(B, gamma_max, V, dtype)) return SV_ERR_BAD_SHAPE;
   const int G = gamma_max;
+  if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
+  if (!sizes_ok(B, G, V, dtype)) return SV_ERR_BAD_SHAPE;
   if (!target_logits || !temperature || !uniforms || !out_tokens || !out_num_emitted)
     return SV_ERR_NULL_POINTER;
   if (G > 0 && (!draft_logits || !draft_tokens)) return SV_ERR_NULL_POINTER;
-  const bool bf16 = dtype == SV_DTYPE_BF16;
-  const uintptr_t es = bf16 ? 2 : 4;
-  auto mis = [](const void* p, uintptr_t a) { return p && (reinterpret_cast<uintptr_t>(p) % a) != 0; };
-  if (mis(draft_tokens, 4) || mis(draft_len, 4) || mis(temperature, 4) || mis(top_k, 4) ||
-      mis(top_p, 4) || mis(uniforms, 4) || mis(out_tokens, 4) || mis(out_num_emitted, 4) ||
-      mis(out_alpha, 4) || mis(out_p_draft, 4) || mis(out_q_draft, 4) || mis(workspace, 16))
-    return SV_ERR_MISALIGNED;
-  // Rows of 16-byte multiples on 16-byte aligned bases only.
-  if ((static_cast<size_t>(V) * es) % 16 != 0) return SV_ERR_BAD_SHAPE;
-  if (mis(target_logits, 16) || mis(draft_logits, 16)) return SV_ERR_MISALIGNED;
+  if (workspace && reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SV_ERR_MISALIGNED;
+  const void* p4[] = {draft_tokens, draft_len, temperature, top_k, top_p, uniforms, out_tokens,
+                      out_num_emitted, out_alpha, out_p_draft, out_q_draft};
+  int sC = 0;
+  const int st = filter_args_status(target_logits, draft_logits, p4, 11, B, G, V, dtype, &sC);
+  if (st != SV_OK) return st;
   const size_t need = spec_verify_workspace_size(B, G, V, dtype);
   if (!workspace || workspace_bytes < need) return SV_ERR_WORKSPACE_TOO_SMALL;
-  if (static_cast<long long>(B) * (G + 1) > INT_MAX / sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
-  const int units = static_cast<int>(static_cast<size_t>(V) * es / 16);
-  int C = 1;
-  while ((units + C - 1) / C > sv::filter_max_row_units()) {
-    if (C >= sv::kMaxCluster) return SV_ERR_BAD_SHAPE;
-    C *= 2;
-  }
   int dev = 0;
   const int dev_status = check_device(&dev);
   if (dev_status != SV_OK) return dev_status;
 
+  const bool bf16 = dtype == SV_DTYPE_BF16;
+  const long long row_bytes = static_cast<long long>(V) * (bf16 ? 2 : 4);
   sv::Params P{};
   P.zt = target_logits;
   P.zd = draft_logits;
@@ -429,34 +485,27 @@ int spec_verify_filtered(const void* target_logits, const void* draft_logits,
   P.rec = reinterpret_cast<int2*>(ws);
   P.cnt = reinterpret_cast<unsigned*>(ws + records_bytes(B, G));
   P.status = P.cnt + B;
+  float* tau = reinterpret_cast<float*>(ws + thresholds_offset(B, G));
   P.B = B;
   P.G = G;
   P.V = V;
-  P.units = units;
-  P.C = C;
-  P.per = (units + C - 1) / C;
-  int maxc = 0;
-  if (max_clusters(dev, bf16, C, &maxc, true) != SV_OK) return SV_ERR_CUDA;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  // 1. The threshold of every row a filter touches (-inf for the others).
+  unsigned* row_counter = reinterpret_cast<unsigned*>(tau + threshold_rows_of(B, G));
+  if (sv::launch_threshold(P, bf16, tau, row_counter, stream) != cudaSuccess) return SV_ERR_CUDA;
+  // 2. The streaming kernel with every logit below its row's threshold read as -inf.
+  P.tau = tau;
   const long long slots = static_cast<long long>(B) * (G + 1);
+  P.units = static_cast<int>(row_bytes / 16);
+  P.C = stream_plan_C(dev, bf16, row_bytes, slots, sC);
+  P.per = (P.units + P.C - 1) / P.C;
+  int maxc = 0;
+  if (max_clusters(dev, bf16, P.C, &maxc, true) != SV_OK) return SV_ERR_CUDA;
   P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
-  // Rows whose filters keep every token, and greedy rows, run on the streaming kernel (the same
-  // outputs as spec_verify_ex, without the filter kernel's selections); the filter kernel takes
-  // the others. Both write disjoint rows of the same outputs and workspace.
-  const long long row_bytes = static_cast<long long>(V) * static_cast<long long>(es);
-  const int sC = stream_cluster_size(row_bytes, bf16);
-  if (sC > 0) {
-    sv::Params S = P;
-    S.C = stream_plan_C(dev, bf16, row_bytes, slots, sC);
-    S.per = (S.units + S.C - 1) / S.C;
-    int smax = 0;
-    if (max_clusters(dev, bf16, S.C, &smax) != SV_OK) return SV_ERR_CUDA;
-    S.nclusters = static_cast<int>(slots < smax ? slots : smax);
-    S.split = 1;
-    P.split = 1;
-    if (sv::launch_stream(S, bf16, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
-      return SV_ERR_CUDA;
-  }
-  if (sv::launch_filter(P, bf16, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+  if (sv::launch_stream(P, bf16, stream) != cudaSuccess) return SV_ERR_CUDA;
+  // 3. Leave the workspace zeroed: a later call of other sizes keeps its counters where these
+  //    thresholds and the row counter were.
+  if (cudaMemsetAsync(tau, 0, need - thresholds_offset(B, G), stream) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
 }

@@ -69,12 +69,12 @@ struct Params {
   int32_t* out_path;         // [B, N] longest accepted path, root first
   int32_t* out_plen;         // [B] nodes on the path
   int32_t* out_pred;         // [B, N] target argmax per node, or null
-  // Filtered verification (filter kernel): per-row top-k and top-p, applied to p and q alike.
+  // Filtered verification: per-row top-k and top-p, applied to p and q alike.
   const int32_t* top_k;      // [B] or null (0 or >= V: off)
   const float* top_p;        // [B] or null (>= 1: off)
-  // Filtered verification in two launches (split != 0): the streaming kernel takes the rows that
-  // row_unfiltered picks, the filter kernel the others.
-  int split;
+  // Filtered verification by thresholds: per row the smallest logit the filters keep (target rows
+  // [B, G+1], then draft rows [B, G]); the streaming kernel reads every logit below it as -inf.
+  const float* tau;
 };
 
 constexpr int kMaxTreeNodes = 65;    // N <= SV_MAX_GAMMA + 1
@@ -180,6 +180,27 @@ __device__ __forceinline__ float vec_get(const uint4& v, int e) {
   const uint32_t x = w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
   if (BF16) return __uint_as_float((e & 1) ? (x & 0xffff0000u) : (x << 16));
   return __uint_as_float(x);
+}
+
+// The vector with every logit below tau read as -inf (NaN stays: it still marks a bad row). tau is a
+// stored logit value (exact in the storage type) or -inf.
+template <bool BF16>
+__device__ __forceinline__ uint4 mask_below(const uint4& v, float tau) {
+  if (BF16) {
+    const uint32_t t = __float_as_uint(tau) >> 16;
+    const uint32_t t2 = t | (t << 16);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t m;
+      asm("set.lt.u32.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w[q]), "r"(t2));   // 0xffff where z < tau
+      w[q] = (w[q] & ~m) | (0xff80ff80u & m);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  const uint32_t ninf = 0xff800000u;
+  return make_uint4(__uint_as_float(v.x) < tau ? ninf : v.x, __uint_as_float(v.y) < tau ? ninf : v.y,
+                    __uint_as_float(v.z) < tau ? ninf : v.z, __uint_as_float(v.w) < tau ? ninf : v.w);
 }
 
 // NaN-propagating max of the logits of a 16-byte vector.
@@ -523,16 +544,6 @@ __device__ __forceinline__ float p_vec_sum(const uint4& t, float k, float cb) {
 // Row scalars and row errors
 // ------------------------------------------------------------------------------------------------
 
-// A row whose filters keep every token (top_k off or >= V, top_p >= 1), or a greedy row (the
-// filters keep its argmax): the same outputs as without filters. A NaN or non-positive top_p is
-// not unfiltered (the filter kernel reports it as a row error).
-__device__ __forceinline__ bool row_unfiltered(const Params& P, int b) {
-  if (__ldg(P.temperature + b) == 0.0f) return true;
-  const int k = P.top_k ? __ldg(P.top_k + b) : 0;
-  const float pp = P.top_p ? __ldg(P.top_p + b) : 1.0f;
-  return (k <= 0 || k >= P.V) && pp >= 1.0f;
-}
-
 // Writes the all-error outputs of row b (one full warp).
 __device__ __forceinline__ void write_row_error(const Params& P, int b, int lane) {
   const int G = P.G;
@@ -578,6 +589,8 @@ struct Pos {
 // Slot s in position-major order (s = i * B + b): the slots a cluster strides over mix every
 // position index, so ragged rows (fewer positions at large i) and the cheaper bonus positions
 // spread evenly over the clusters.
+// kMask: a filtered launch, where a sampled row also needs top_p > 0.
+template <bool kMask = false>
 __device__ __forceinline__ Pos classify(const Params& P, int s) {
   Pos p;
   p.i = s / P.B;
@@ -599,9 +612,12 @@ __device__ __forceinline__ Pos classify(const Params& P, int s) {
   p.load = p.len_ok && p.t_ok && p.i <= p.gb;
   p.two = p.load && !p.greedy && p.i < p.gb && !P.onehot;
   p.oh = p.load && !p.greedy && p.i < p.gb && P.onehot;
-  if (P.split && !row_unfiltered(P, p.b)) {   // the filter kernel's row: no work, no error here
-    p.len_ok = p.t_ok = true;
-    p.load = p.two = p.oh = false;
+  if (kMask && !p.greedy && P.top_p) {
+    const float pp = __ldg(P.top_p + p.b);
+    if (!(pp > 0.0f)) {                        // NaN fails too
+      p.t_ok = false;
+      p.load = p.two = p.oh = false;
+    }
   }
   return p;
 }
@@ -804,10 +820,11 @@ __device__ __forceinline__ float group_sum(float v) {
 // group sums, then one reload of the crossing group. Returns the token in warp `finisher` (all its
 // lanes); other warps return -1. All consumer threads call it. Token `skip_tok` (if >= 0) has weight 0
 // (the usum entries already leave it out).
-template <bool BF16, int kGrp, int kNT, int kBarId, typename SM>
+template <bool BF16, int kGrp, int kNT, int kBarId, bool kMask = false, typename SM>
 __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, const char* rowt,
                           const char* rowd, bool resid, float k, float ct, float cd, float cb,
-                          SM& sm, int ctid, int& finisher, int skip_tok = -1) {
+                          SM& sm, int ctid, int& finisher, int skip_tok = -1,
+                          float tau_t = -INFINITY, float tau_d = -INFINITY) {
   constexpr int kCT = kNT, kCW = kNT / 32;
   constexpr int E = BF16 ? 8 : 4;
   const int lane = ctid & 31, cw = ctid >> 5;
@@ -888,7 +905,9 @@ __device__ int chunk_draw(const float* usum, int cu, int u0, float t_local, cons
     for (int u = ga; u < gz && (pick < 0 || overrun); ++u) {
       uint4 t = ld_stream_v4(reinterpret_cast<const uint4*>(rowt) + u);
       if (skip_tok >= 0 && u == skip_tok / E) t = mask_elem<BF16>(t, skip_tok - u * E);   // weight 0
-      const uint4 d = resid ? ld_stream_v4(reinterpret_cast<const uint4*>(rowd) + u) : t;
+      if (kMask) t = mask_below<BF16>(t, tau_t);                  // filtered rows
+      uint4 d = resid ? ld_stream_v4(reinterpret_cast<const uint4*>(rowd) + u) : t;
+      if (kMask && resid) d = mask_below<BF16>(d, tau_d);
 #pragma unroll
       for (int e = 0; e < E; e += 2) {
         float w0, w1;
@@ -932,12 +951,14 @@ int verify_args_status(const void* target_logits, const void* draft_logits,
 cudaError_t launch_element(const Params& P, bool bf16, int vpt_index, cudaStream_t stream);
 // Streaming path (16-byte aligned rows): persistent clusters fed by bulk copies.
 cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream);
-// Clusters of `C` CTAs of the streaming kernel that fit on the current device at once.
-cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n);
-// Filtered verification (16-byte aligned rows of at most 16 chunks of filter_max_row_units()
-// vectors): persistent clusters, one position per cluster at a time.
-cudaError_t launch_filter(Params P, bool bf16, cudaStream_t stream);
-cudaError_t filter_max_clusters(bool bf16, int C, int* n);
-int filter_max_row_units();
+// Clusters of `C` CTAs of the streaming kernel that fit on the current device at once (masked: the
+// instantiation of filtered verification).
+cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n, bool masked = false);
+// Per-row thresholds of top-k / top-p filtering (16-byte aligned rows): tau [B * (2G + 1)], target
+// rows [B, G+1] then draft rows [B, G]. rows: a zeroed device counter the CTAs claim rows from (it
+// ends at rows + grid size), or null for a static split.
+int threshold_rows(const Params& P);
+cudaError_t launch_threshold(const Params& P, bool bf16, float* tau, unsigned* rows,
+                             cudaStream_t stream);
 
 }  // namespace sv

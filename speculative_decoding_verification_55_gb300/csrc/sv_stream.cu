@@ -152,7 +152,7 @@ struct Shared {
     const char* rt;
     const char* rd;
     int b, i, gb, acc, bad, p_chunk, fin;
-    float k, ct, cd, cb, px, qx, p_tlocal, u_res;
+    float k, ct, cd, cb, px, qx, p_tlocal, u_res, tau_t, tau_d;
   } pend;
 };
 
@@ -164,7 +164,10 @@ __device__ __forceinline__ void set_status(const Params& P, Shared& sm, unsigned
 // Bytes every CTA pushes into every CTA of its cluster per exchange: one float4 record and one uint2.
 constexpr uint32_t kXchBytes = 24;
 
-template <bool BF16, int kGrp>
+// kMask: filtered verification. Every logit below its row's threshold P.tau reads as -inf (the
+// thresholds come from the threshold kernel): the softmax of the kept logits is the filtered
+// distribution, and the rest of the path is unchanged.
+template <bool BF16, int kGrp, bool kMask>
 __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Shared sm;
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       return false;
     };
     for (int s = cid; s < total && ok; s += P.nclusters) {
-      const Pos p = classify(P, s);
+      const Pos p = classify<kMask>(P, s);
       if (!p.load) continue;
       for (int row = 0; row < (p.two ? 2 : 1) && ok; ++row) {
         const char* g = row == 0
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
 
   // Group sums of p's unnormalised weights exp2(z k + cb) over this CTA's chunk, from L2; token
   // `excl` (if >= 0) left out.
-  auto fill_p_sums = [&](const char* rt, float kk, float cbv, int excl) {
+  auto fill_p_sums = [&](const char* rt, float kk, float cbv, int excl, float tau_r = -INFINITY) {
     const uint4* vt = reinterpret_cast<const uint4*>(rt) + u0;
     const int xu = excl >= 0 ? excl / E - u0 : -1;     // the chunk-local vector holding excl
     int base = 0;
@@ -296,6 +299,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       for (int j = 0; j < 8; ++j) {
         t[j] = ld_stream_v4(vt + base + ctid + j * kCT);
         if (base + ctid + j * kCT == xu) t[j] = mask_elem<BF16>(t[j], excl - (u0 + xu) * E);
+        if (kMask) t[j] = mask_below<BF16>(t[j], tau_r);
       }
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -309,6 +313,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       if (uu < cu) {
         uint4 t = ld_stream_v4(vt + uu);
         if (uu == xu) t = mask_elem<BF16>(t, excl - (u0 + xu) * E);
+        if (kMask) t = mask_below<BF16>(t, tau_r);
         sv = p_vec_sum<BF16>(t, kk, cbv);
       }
       const float g = group_sum<kGrp>(sv);
@@ -506,19 +511,20 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
     const char* prt = sm.pend.rt;
     const char* prd = sm.pend.rd;
     const float pkk = sm.pend.k, pct = sm.pend.ct, pcd = sm.pend.cd, pcb = sm.pend.cb;
+    const float ptt = sm.pend.tau_t, ptd = sm.pend.tau_d;
     if (!resid) {
-      fill_p_sums(prt, pkk, pcb, -1);
+      fill_p_sums(prt, pkk, pcb, -1, ptt);
       named_bar_sync(kConsumerBar, kCT);
     }
     int finisher = 0;
-    const int tok = chunk_draw<BF16, kGrp, kCT, kConsumerBar>(usum, cu, u0, tl, prt, prd, resid, pkk, pct, pcd, pcb, sm,
-                                           ctid, finisher);
+    const int tok = chunk_draw<BF16, kGrp, kCT, kConsumerBar, kMask>(usum, cu, u0, tl, prt, prd, resid, pkk, pct, pcd, pcb, sm,
+                                           ctid, finisher, -1, ptt, ptd);
     if (cw == finisher) finish_position(P, pb, pi, pgb, tok, tok < 0 ? kFlagBad : 0, alpha, ppx, pqx,
                                         lane);
   };
 
   for (int s = cid; s < total; s += P.nclusters) {
-    const Pos p = classify(P, s);
+    const Pos p = classify<kMask>(P, s);
     if (!p.load) {
       if (!(p.len_ok && p.t_ok) && p.i == 0 && rank == 0 && cw == 0) {
         if (P.tree) write_tree_row_error(P, p.b, lane);
@@ -534,6 +540,12 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
                              : nullptr;
     const int x = (!P.tree && p.i < p.gb) ? __ldg(P.tokens + (size_t)p.b * G + p.i) : -1;
 
+    // Filtered rows: the thresholds of this position's rows (-inf: nothing dropped).
+    float tau_t = -INFINITY, tau_d = -INFINITY;
+    if (kMask) {
+      tau_t = __ldg(P.tau + (size_t)p.b * G1 + p.i);
+      if (p.two) tau_d = __ldg(P.tau + (size_t)P.B * G1 + (size_t)p.b * G + p.i);
+    }
     // Early scalar loads for the accept test (their latency hides behind pass 1).
     float zx_t = 0.0f, zx_d = 0.0f, u_acc = 0.0f, u_res = 0.0f, u_bon = 0.0f;
     if (ok && cw == 0 && !p.greedy) {
@@ -545,6 +557,10 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         zx_t = load_logit<BF16>(rowt, x);
       }
       if (kind == kVerify) zx_d = load_logit<BF16>(rowd, x);
+      if (kMask) {                 // a drafted token outside a filtered set has probability 0
+        if (zx_t < tau_t) zx_t = -INFINITY;
+        if (zx_d < tau_d) zx_d = -INFINITY;
+      }
     }
 
     // ---- pass 1 out of the ring ----
@@ -572,6 +588,11 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
               const int uu = ctid + j * kCT;
               v[j] = uu < nu ? src[uu] : make_uint4(ninf, ninf, ninf, ninf);
             }
+          }
+          if (kMask && kind != kArgmax) {
+            const float tr = row == 0 ? tau_t : tau_d;
+#pragma unroll
+            for (int j = 0; j < N; ++j) v[j] = mask_below<BF16>(v[j], tr);
           }
           if (kind == kOneHot) {
             // The drafted token's own term is added at the exchange: the chunk sums leave it out,
@@ -698,7 +719,7 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
         fill_p_sums(rowt, kk, cb, x);
         named_bar_sync(kConsumerBar, kCT);
         int finisher = 0;
-        const int tok = chunk_draw<BF16, kGrp, kCT, kConsumerBar>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm,
+        const int tok = chunk_draw<BF16, kGrp, kCT, kConsumerBar, kMask>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm,
                                                ctid, finisher, x);
         if (cw == finisher)
           finish_position(P, p.b, p.i, p.gb, tok, tok < 0 ? kFlagBad : 0, apx, apx, 1.0f, lane);
@@ -722,11 +743,11 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
           if (cw == 0) finish_position(P, p.b, p.i, p.gb, -1, kFlagAccept, 0.0f, 0.0f, 0.0f, lane);
           continue;
         }
-        fill_p_sums(rowt, kk, cb, -1);
+        fill_p_sums(rowt, kk, cb, -1, tau_t);
         named_bar_sync(kConsumerBar, kCT);
         int finisher = 0;
-        const int tok = chunk_draw<BF16, kGrp, kCT, kConsumerBar>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm,
-                                               ctid, finisher);
+        const int tok = chunk_draw<BF16, kGrp, kCT, kConsumerBar, kMask>(usum, cu, u0, tl, rowt, rowd, false, kk, ct, cd, cb, sm,
+                                               ctid, finisher, -1, tau_t);
         if (cw == finisher)
           finish_position(P, p.b, p.i, p.gb, tok, (tok < 0 ? kFlagBad : 0) | kFlagAccept, 0.0f, 0.0f,
                           0.0f, lane);
@@ -753,7 +774,15 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
 #pragma unroll
           for (int j = 0; j < kHalfUnits / kCT; ++j) {
             const int uu = ctid + j * kCT;
-            const float sv = uu < nu ? resid_vec_sum<BF16>(st4[uu], sd4[uu], k2, c2) : 0.0f;
+            float sv = 0.0f;
+            if (uu < nu) {
+              if (kMask) {
+                sv = resid_vec_sum<BF16>(mask_below<BF16>(st4[uu], tau_t),
+                                         mask_below<BF16>(sd4[uu], tau_d), k2, c2);
+              } else {
+                sv = resid_vec_sum<BF16>(st4[uu], sd4[uu], k2, c2);
+              }
+            }
             W += sv;
             const float g = group_sum<kGrp>(sv);
             if ((ctid & (kGrp - 1)) == 0 && uu < nu) usum[(blk * kHalfUnits + uu) / kGrp] = g;
@@ -787,6 +816,10 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
       sm.pend.p_tlocal = sm.p_tlocal;
       sm.pend.u_res = u_res;
       sm.pend.fin = fin;
+      if (kMask) {
+        sm.pend.tau_t = tau_t;
+        sm.pend.tau_d = tau_d;
+      }
     }
   }
   if (pv && !sm.stop_snap) {
@@ -805,13 +838,18 @@ __global__ void __launch_bounds__(kThreadsS, kCtasPerSm<BF16>) sv_stream_kernel(
   cluster_sync_all();
 }
 
-// bf16 one-hot launches take the wide draw groups; the rest the narrow ones.
-const void* stream_fn(bool bf16, bool wide) {
-  if (bf16) {
-    return wide ? reinterpret_cast<const void*>(sv_stream_kernel<true, kGrpWide>)
-                : reinterpret_cast<const void*>(sv_stream_kernel<true, kGrpNarrow>);
+// bf16 one-hot launches take the wide draw groups; the rest the narrow ones. Filtered launches
+// (thresholds given) take the masked instantiation.
+const void* stream_fn(bool bf16, bool wide, bool masked = false) {
+  if (masked) {
+    return bf16 ? reinterpret_cast<const void*>(sv_stream_kernel<true, kGrpNarrow, true>)
+                : reinterpret_cast<const void*>(sv_stream_kernel<false, kGrpNarrow, true>);
   }
-  return reinterpret_cast<const void*>(sv_stream_kernel<false, kGrpNarrow>);
+  if (bf16) {
+    return wide ? reinterpret_cast<const void*>(sv_stream_kernel<true, kGrpWide, false>)
+                : reinterpret_cast<const void*>(sv_stream_kernel<true, kGrpNarrow, false>);
+  }
+  return reinterpret_cast<const void*>(sv_stream_kernel<false, kGrpNarrow, false>);
 }
 
 int stream_dyn_bytes(bool bf16, bool wide) {
@@ -849,9 +887,9 @@ cudaLaunchConfig_t stream_config(int C, int nclusters, bool bf16, bool wide, cud
 
 }  // namespace
 
-cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n) {
-  wide = wide && bf16;
-  const void* fn = stream_fn(bf16, wide);
+cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n, bool masked) {
+  wide = wide && bf16 && !masked;
+  const void* fn = stream_fn(bf16, wide, masked);
   const cudaError_t e = stream_attrs(fn, C, bf16, wide);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
@@ -860,8 +898,9 @@ cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n) {
 }
 
 cudaError_t launch_stream(Params P, bool bf16, cudaStream_t stream) {
-  const bool wide = bf16 && P.onehot;
-  const void* fn = stream_fn(bf16, wide);
+  const bool masked = P.tau != nullptr;
+  const bool wide = bf16 && P.onehot && !masked;
+  const void* fn = stream_fn(bf16, wide, masked);
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = stream_config(P.C, P.nclusters, bf16, wide, stream, attr);
   void* args[] = {&P};

@@ -337,10 +337,10 @@ def test_gpu_filtered_token_outside_both_kept_sets(sv, dtype):
 @pytest.mark.gpu
 @pytest.mark.parametrize("dtype,V", [("bf16", 100000), ("f32", 40000)])
 def test_gpu_filtered_candidate_lists(sv, dtype, V):
-    """Top-k rows whose candidates (every logit in the value bin of the k-th largest or above) are
-    gathered into one list: a list of exactly 1024 entries (the capacity) spread over the chunks and
-    held by the last chunk alone, 1025 entries (too many: the chunk-wide selection), a k-th largest
-    far below the max (below the counted bins), top-k with top-p, and a bonus-only row."""
+    """Selections the threshold kernel makes by bins and then radix levels over the logits' keys:
+    1024 and 1025 ties at the max spread over the row, 1024 ties in the last vectors of the row, a
+    k-th largest 57 log2 units below the max (a deep bin), one past 64 log2 units (the tail bin,
+    row 0), top-k with top-p, and a bonus-only row."""
     B, G = 8, 3
     rng = np.random.default_rng(V)
     zt = (rng.standard_normal((B, G + 1, V)) * 2.0).astype(np.float32)
@@ -360,6 +360,10 @@ def test_gpu_filtered_candidate_lists(sv, dtype, V):
     zd[4] = -40.0
     zt[4, :, [3, V // 2, V - 5]] = 0.0
     zd[4, :, [3, V // 2, V - 5]] = 0.0
+    zt[0] = -100.0 + rng.standard_normal((G + 1, V)).astype(np.float32)   # the k-th largest in
+    zd[0] = -100.0 + rng.standard_normal((G, V)).astype(np.float32)       # the tail bin
+    zt[0, :, [7, V // 3, V - 9]] = 0.0
+    zd[0, :, [7, V // 3, V - 9]] = 0.0
     n[6] = 0                                # the bonus position only
     if dtype == "bf16":
         zt, zd = bf16_round(zt), bf16_round(zd)
@@ -374,6 +378,71 @@ def test_gpu_filtered_candidate_lists(sv, dtype, V):
     gpu = run_filtered(sv, zt, zd, x, n, T, u, top_k, top_p, dtype)
     rep, skipped = check_filtered(zt, zd, x, n, T, u, top_k, top_p, gpu)
     assert skipped <= 2, skipped
+
+
+def smallest_kept(z, T, k, top_p):
+    """The smallest logit the oracle's filters keep, for a row of finite logits (every logit has
+    probability > 0, so the kept set is where the filtered probability is positive)."""
+    assert np.isfinite(z).all()
+    pk, _ = filtered_softmax(z, T, int(k), np.float64(top_p))
+    return float(np.asarray(z, np.float64)[pk > 0].min())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,V", [("f32", 4100), ("bf16", 32000), ("bf16", 256000)])
+def test_gpu_thresholds_are_the_smallest_kept_logit(sv, dtype, V):
+    """spec_verify_filter_thresholds: for every filtered row read by the round, the smallest logit
+    the oracle's filters keep (exact: it is one of the row's logits); -inf for greedy rows, rows
+    that are not read, rows whose filters are off and rows with a bad top_p."""
+    B, G = 10, 3
+    zt, zd, x, n, T, u, top_k, top_p = filter_batch(B, G, V, dtype, seed=V + 3, greedy_frac=0.2)
+    top_p[B - 1] = 0.0                      # a row error of spec_verify_filtered: -inf
+    zt, zd = np.nan_to_num(zt, nan=0.0), np.nan_to_num(zd, nan=0.0)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
+    nt = B * (2 * G + 1)
+    out = torch.full((nt,), 7.0, dtype=torch.float32, device="cuda")
+    sv.spec_verify_filter_thresholds(dev(zt).to(tdt), dev(zd).to(tdt), dev(n), dev(T), dev(top_k),
+                                     dev(top_p), out)
+    torch.cuda.synchronize()
+    tau = out.cpu().numpy()
+    checked = 0
+    for r in range(nt):
+        draft = r >= B * (G + 1)
+        b, i = divmod(r - B * (G + 1), G) if draft else divmod(r, G + 1)
+        read = i < n[b] if draft else i <= n[b]
+        on = (0 < top_k[b] < V) or top_p[b] < 1.0
+        if not (read and T[b] > 0 and on and top_p[b] > 0):
+            assert tau[r] == -np.inf, (r, tau[r])
+            continue
+        z = (zd if draft else zt)[b, i]
+        _, margin = filtered_softmax(z, T[b], int(top_k[b]), np.float64(top_p[b]))
+        if margin < TOL:
+            continue
+        assert tau[r] == np.float32(smallest_kept(z, T[b], top_k[b], top_p[b])), (r, b, i, tau[r])
+        checked += 1
+    assert checked >= 5
+
+
+@pytest.mark.gpu
+def test_gpu_filtered_workspace_reused_across_sizes(sv):
+    """One workspace serves calls of different sizes: a filtered call leaves every byte of it zero
+    (its thresholds lie where another size keeps records and counters), so the next call of other
+    sizes on the same workspace still verifies correctly."""
+    dtc = sv.SV_DTYPE_F32
+    big = sv.spec_verify_workspace_size(64, 8, 4096, dtc)
+    ws = torch.zeros(big, dtype=torch.uint8, device="cuda")
+    for (B, G, V, seed) in ((4, 3, 4096, 1), (12, 3, 4096, 2), (3, 8, 4096, 3), (16, 2, 4096, 4)):
+        zt, zd, x, n, T, u, top_k, top_p = filter_batch(B, G, V, "f32", seed=seed)
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
+        outs = (torch.full((B, G + 1), -7, dtype=torch.int32, device="cuda"),
+                torch.full((B,), -7, dtype=torch.int32, device="cuda"),
+                *[torch.empty((B, G), dtype=torch.float32, device="cuda") for _ in range(3)])
+        sv.spec_verify_filtered(dev(zt), dev(zd), dev(x), dev(n), dev(T), dev(top_k), dev(top_p),
+                                dev(u), *outs, ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0, (B, G)
+        check_filtered(zt, zd, x, n, T, u, top_k, top_p, [o.cpu().numpy() for o in outs])
 
 
 @pytest.mark.gpu
@@ -395,8 +464,8 @@ def test_gpu_filtered_row_errors(sv):
 
 @pytest.mark.gpu
 def test_gpu_filters_off_match_the_plain_kernel(sv):
-    """Filters off (the filter kernel) and top_k / top_p None (the streaming kernel) both match
-    the plain oracle."""
+    """Filters off in every row (thresholds -inf) and top_k / top_p None both match the plain
+    oracle."""
     B, G, V = 16, 4, 32000
     zt, zd, x, n, T, u, _, _ = filter_batch(B, G, V, "bf16", seed=9)
     a = run_filtered(sv, zt, zd, x, n, T, u, np.zeros(B, np.int32), np.ones(B, np.float32), "bf16")
