@@ -13,8 +13,8 @@
 // kernel then verifies the batch with every logit below its row's threshold read as -inf: the
 // softmax of the kept logits is the renormalised filtered distribution.
 //
-// One CTA of 1024 threads per row at a time (persistent over the rows, one CTA per SM); nothing is
-// shared between CTAs. Masses are w = 2^-d with d = (M - z) log2(e) / T the logit's log2
+// One CTA of 512 threads per row at a time (persistent over the rows, two CTAs per SM, so that one
+// streams while the other selects); nothing is shared between CTAs. Masses are w = 2^-d with d = (M - z) log2(e) / T the logit's log2
 // probability below the row max M. Per row:
 //   1  one pass over the row: M, and a strided sample of the row's vectors kept in shared memory.
 //   2  the sample's histogram over fine bins of d (8 per unit over [0, 64), then a tail bin) gives
@@ -37,7 +37,8 @@
 namespace sv {
 namespace {
 
-constexpr int kTT = 1024;                 // threads per CTA
+constexpr int kTT = 512;                  // threads per CTA
+constexpr int kCtasT = 2;                 // CTAs per SM: one streams while the other selects
 constexpr int kTW = kTT / 32;
 constexpr int kFB = 512;                  // fine bins (bin kFB is the tail)
 constexpr float kFBPerLog2 = 8.0f;        // fine bins per unit of log2 probability
@@ -47,6 +48,7 @@ constexpr float kFix = 4398046511104.0f;  // 2^42: the fixed-point scale of a ma
 constexpr int kSampleVecs = 2048;         // sampled 16-byte vectors at most
 constexpr int kCandMax = 16384;           // candidate logits (fp32)
 constexpr int kU = 2;                     // vectors in flight per thread in the two passes
+constexpr int kWarpSolve = 2048;          // candidate lists up to this length: one warp selects
 
 // Dynamic shared memory holds either the fast path's sample and candidates or the exact path's
 // per-warp level-0 histograms (never both at once).
@@ -285,11 +287,14 @@ __device__ __forceinline__ int warp_last_below(const unsigned* cnt, const unsign
   return __shfl_sync(kFull, jsel, L);
 }
 
-// Block-wide sums (every thread calls; every thread gets the totals).
-__device__ __forceinline__ void block_sum2(TShared& sm, unsigned long long& a, unsigned long long& b,
+// Group-wide sums over kN threads (kN = 32: one warp, no shared memory; kN = kTT: the CTA, in warp
+// order so the sums are the same every run). Every thread of the group calls; every one gets them.
+template <int kN>
+__device__ __forceinline__ void group_sum2(TShared& sm, unsigned long long& a, unsigned long long& b,
                                            int lane, int warp) {
   a = warp_sum(a);
   b = warp_sum(b);
+  if (kN == 32) return;
   if (lane == 0) {
     sm.redm[warp] = a;
     sm.redm2[warp] = b;
@@ -298,11 +303,25 @@ __device__ __forceinline__ void block_sum2(TShared& sm, unsigned long long& a, u
   a = 0;
   b = 0;
 #pragma unroll 8
-  for (int w = 0; w < kTW; ++w) {     // warp order: the same sums every run
+  for (int w = 0; w < kTW; ++w) {
     a += sm.redm[w];
     b += sm.redm2[w];
   }
   __syncthreads();
+}
+
+__device__ __forceinline__ void block_sum2(TShared& sm, unsigned long long& a, unsigned long long& b,
+                                           int lane, int warp) {
+  group_sum2<kTT>(sm, a, b, lane, warp);
+}
+
+template <int kN>
+__device__ __forceinline__ void group_sync() {
+  if (kN == 32) {
+    __syncwarp();
+  } else {
+    __syncthreads();
+  }
 }
 
 template <bool BF16>
@@ -315,20 +334,20 @@ struct RowCtx {
   bool kon, pon;
 };
 
-// ---- radix levels over the candidate list (fast path) ----
-// Candidates that take part: class test `in_set` (by fine bin) and key >= kmin. Counts (and
-// masses) per sub-range of 2^shift keys inside [kl, kl + 2^(shift + 8)).
-template <bool BF16, typename InSet>
+// ---- radix levels over the candidate list (fast path), by a group of kN threads ----
+// Candidates that take part: class test `in_set` and key >= kmin. Counts (and masses) per
+// sub-range of 2^shift keys inside [kl, kl + 2^(shift + 8)).
+template <int kN, bool BF16, typename InSet>
 __device__ __forceinline__ void cand_level(TShared& sm, const float* cand, int nc, uint32_t kl,
                                            int shift, uint32_t kmin, bool masses, float Mk, float k,
                                            InSet in_set, int tid) {
-  for (int j = tid; j < 256; j += kTT) {
+  for (int j = tid; j < 256; j += kN) {
     sm.rc[j] = 0u;
     sm.rm[j] = 0ull;
   }
-  __syncthreads();
+  group_sync<kN>();
   const unsigned long long span = 256ull << shift;
-  for (int i = tid; i < nc; i += kTT) {
+  for (int i = tid; i < nc; i += kN) {
     const float z = cand[i];
     const uint32_t key = order_key<BF16>(z);
     const unsigned long long off = static_cast<unsigned long long>(key) - kl;
@@ -338,17 +357,17 @@ __device__ __forceinline__ void cand_level(TShared& sm, const float* cand, int n
       if (masses) atomicAdd(&sm.rm[s], fix_mass(z, Mk, k));
     }
   }
-  __syncthreads();
+  group_sync<kN>();
 }
 
 // The smallest candidate key in the set (>= kmin) and the first radix shift: levels of 8 bits from
 // that key cover the set's key span (one level when it spans fewer than 256 keys).
-template <bool BF16, typename InSet>
+template <int kN, bool BF16, typename InSet>
 __device__ __forceinline__ uint32_t cand_key_range(TShared& sm, const float* cand, int nc,
                                                    uint32_t kmin, InSet in_set, int tid, int lane,
                                                    int warp, int& shift0) {
   uint32_t lo = 0xffffffffu, hi = 0u;
-  for (int i = tid; i < nc; i += kTT) {
+  for (int i = tid; i < nc; i += kN) {
     const float z = cand[i];
     const uint32_t key = order_key<BF16>(z);
     if (key >= kmin && in_set(z)) {
@@ -358,19 +377,21 @@ __device__ __forceinline__ uint32_t cand_key_range(TShared& sm, const float* can
   }
   lo = __reduce_min_sync(kFull, lo);
   hi = __reduce_max_sync(kFull, hi);
-  if (lane == 0) {
-    sm.redu[warp] = lo;
-    sm.redm[warp] = hi;
-  }
-  __syncthreads();
-  lo = 0xffffffffu;
-  hi = 0u;
+  if (kN != 32) {
+    if (lane == 0) {
+      sm.redu[warp] = lo;
+      sm.redm[warp] = hi;
+    }
+    __syncthreads();
+    lo = 0xffffffffu;
+    hi = 0u;
 #pragma unroll 8
-  for (int w = 0; w < kTW; ++w) {
-    lo = min(lo, sm.redu[w]);
-    hi = max(hi, static_cast<uint32_t>(sm.redm[w]));
+    for (int w = 0; w < kTW; ++w) {
+      lo = min(lo, sm.redu[w]);
+      hi = max(hi, static_cast<uint32_t>(sm.redm[w]));
+    }
+    __syncthreads();
   }
-  __syncthreads();
   if (lo > hi) lo = hi = kmin;                     // an empty set
   const uint32_t span = hi - lo;
   const int bits = span ? 32 - __clz(span) : 0;
@@ -379,55 +400,97 @@ __device__ __forceinline__ uint32_t cand_key_range(TShared& sm, const float* can
 }
 
 // The k-th largest key among the candidates in the set (rank k counted from the top).
-template <bool BF16, typename InSet>
+template <int kN, bool BF16, typename InSet>
 __device__ uint32_t cand_kth(TShared& sm, const float* cand, int nc, int rank, float Mk, float k,
                              InSet in_set, int tid, int lane, int warp) {
   int shift0 = 0;
-  uint32_t kl = cand_key_range<BF16>(sm, cand, nc, 0u, in_set, tid, lane, warp, shift0);
+  uint32_t kl = cand_key_range<kN, BF16>(sm, cand, nc, 0u, in_set, tid, lane, warp, shift0);
   for (int shift = shift0; shift >= 0; shift -= 8) {
-    cand_level<BF16>(sm, cand, nc, kl, shift, 0u, false, Mk, k, in_set, tid);
+    cand_level<kN, BF16>(sm, cand, nc, kl, shift, 0u, false, Mk, k, in_set, tid);
+    int s = 0, r2 = rank;
     if (warp == 0) {
       unsigned before = 0, total = 0;
-      const int s = warp_first_reach<8, true, unsigned>(sm.rc, 255, static_cast<unsigned>(rank),
-                                                        lane, before, total);
-      if (lane == 0) {
-        sm.bi[4] = s < 0 ? 0 : s;
-        sm.bi[5] = rank - static_cast<int>(before);
+      s = warp_first_reach<8, true, unsigned>(sm.rc, 255, static_cast<unsigned>(rank), lane, before,
+                                              total);
+      s = s < 0 ? 0 : s;
+      r2 = rank - static_cast<int>(before);
+      if (kN != 32 && lane == 0) {
+        sm.bi[4] = s;
+        sm.bi[5] = r2;
       }
     }
-    __syncthreads();
-    kl += static_cast<uint32_t>(sm.bi[4]) << shift;
-    rank = sm.bi[5];
-    __syncthreads();
+    if (kN != 32) {
+      __syncthreads();
+      s = sm.bi[4];
+      r2 = sm.bi[5];
+      __syncthreads();
+    }
+    kl += static_cast<uint32_t>(s) << shift;
+    rank = r2;
   }
   return kl;
 }
 
 // The smallest key (>= kmin, in the set) whose strictly-larger mass, plus `base`, stays below
 // `target`.
-template <bool BF16, typename InSet>
+template <int kN, bool BF16, typename InSet>
 __device__ uint32_t cand_topp(TShared& sm, const float* cand, int nc, uint32_t kmin,
                               unsigned long long base, double target, float Mk, float k,
                               InSet in_set, int tid, int lane, int warp) {
   int shift0 = 0;
-  uint32_t kl = cand_key_range<BF16>(sm, cand, nc, kmin, in_set, tid, lane, warp, shift0);
+  uint32_t kl = cand_key_range<kN, BF16>(sm, cand, nc, kmin, in_set, tid, lane, warp, shift0);
   unsigned long long above = base;
   for (int shift = shift0; shift >= 0; shift -= 8) {
-    cand_level<BF16>(sm, cand, nc, kl, shift, kmin, true, Mk, k, in_set, tid);
+    cand_level<kN, BF16>(sm, cand, nc, kl, shift, kmin, true, Mk, k, in_set, tid);
+    int s = 0;
+    unsigned long long asel = above;
     if (warp == 0) {
-      unsigned long long asel = 0;
-      const int s = warp_last_below(sm.rc, sm.rm, above, target, lane, asel);
-      if (lane == 0) {
-        sm.bi[6] = s < 0 ? 0 : s;
+      s = warp_last_below(sm.rc, sm.rm, above, target, lane, asel);
+      s = s < 0 ? 0 : s;
+      if (kN != 32 && lane == 0) {
+        sm.bi[6] = s;
         sm.bm[2] = asel;
       }
     }
-    __syncthreads();
-    kl += static_cast<uint32_t>(sm.bi[6]) << shift;
-    above = sm.bm[2];
-    __syncthreads();
+    if (kN != 32) {
+      __syncthreads();
+      s = sm.bi[6];
+      asel = sm.bm[2];
+      __syncthreads();
+    }
+    kl += static_cast<uint32_t>(s) << shift;
+    above = asel;
   }
   return kl > kmin ? kl : kmin;
+}
+
+// The exact selection on the candidate list by a group of kN threads (one warp for a short list,
+// the CTA otherwise). top-k rows: the k-th largest among all candidates, then (top-p) the nucleus of
+// the candidates at or above it. top-p rows: the boundary among T (z >= x_t) or among C (z < x_a)
+// with base mass mT + mA, as the caller decided. Returns the threshold key.
+template <int kN, bool BF16>
+__device__ uint32_t cand_solve(TShared& sm, const float* cand, int nc, bool kon, bool pon, int topk,
+                               float topp, int where, unsigned long long base, double target_p,
+                               float x_t, float x_a, float Mk, float k, int tid, int lane, int warp) {
+  if (kon) {
+    auto all = [](float) { return true; };
+    const uint32_t kth = cand_kth<kN, BF16>(sm, cand, nc, topk, Mk, k, all, tid, lane, warp);
+    if (!pon) return kth;
+    unsigned long long km = 0, unused = 0;
+    for (int j = tid; j < nc; j += kN) {
+      const float z = cand[j];
+      if (order_key<BF16>(z) >= kth) km += fix_mass(z, Mk, k);
+    }
+    group_sum2<kN>(sm, km, unused, lane, warp);
+    const double target = static_cast<double>(topp) * static_cast<double>(km);
+    return cand_topp<kN, BF16>(sm, cand, nc, kth, 0ull, target, Mk, k, all, tid, lane, warp);
+  }
+  if (where == 0) {
+    auto in_t = [=](float z) { return z >= x_t; };
+    return cand_topp<kN, BF16>(sm, cand, nc, 0u, 0ull, target_p, Mk, k, in_t, tid, lane, warp);
+  }
+  auto in_c = [=](float z) { return z < x_a; };
+  return cand_topp<kN, BF16>(sm, cand, nc, 0u, base, target_p, Mk, k, in_c, tid, lane, warp);
 }
 
 // ---- the exact path over the whole row ----
@@ -632,11 +695,12 @@ __device__ __noinline__ uint32_t exact_row(TShared& sm, unsigned char* dyn, cons
 
 // Pass 2 over the row: candidates (cut points of class_words) appended to `cand` in shared memory
 // (warp-aggregated: one atomic per warp and vector step with a candidate), and (kP) the thread's
-// fp32 sum of the masses between the cut points. Every thread calls it with the same trip count.
-template <bool BF16, bool kP>
+// fp32 sum of the masses between the cut points; kMax: also the thread's max (NaN-propagating) in
+// mx. Every thread calls it with the same trip count.
+template <bool BF16, bool kP, bool kMax>
 __device__ __forceinline__ float pass2(TShared& sm, float* cand, const uint4* rv, int nvec, float xt,
                                        float xa, float xl, float Mk, float k, uint64_t pol, int tid,
-                                       int lane) {
+                                       int lane, float& mx) {
   constexpr int E = BF16 ? 8 : 4;
   float s_a = 0.0f;
   for (int u0 = 0; u0 < nvec; u0 += kTT * kU) {
@@ -652,6 +716,7 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, const uint4* rv
       const bool in = u0 + j * kTT + tid < nvec;
       const uint4 v = vv[j];
       uint32_t cw[4], aw[4];
+      if (kMax && in) mx = max_nan(mx, vec_max<BF16>(v));
       class_words<BF16, kP>(v, xt, xa, xl, cw, aw);
       const bool c_any = in && ((cw[0] | cw[1] | cw[2] | cw[3]) != 0u);
       if (kP && in && (aw[0] | aw[1] | aw[2] | aw[3]) != 0u) {
@@ -693,7 +758,7 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, const uint4* rv
 // rows: null, or a zeroed counter from which CTAs claim rows one at a time (rows differ in cost by
 // a few times); without it, CTA c takes rows c, c + gridDim.x, ...
 template <bool BF16>
-__global__ void __launch_bounds__(kTT, 1) sv_threshold_kernel(const Params P, float* tau,
+__global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params P, float* tau,
                                                               unsigned* rows) {
   __shared__ TShared sm;
   extern __shared__ __align__(16) unsigned char dyn_t[];
@@ -753,11 +818,21 @@ __global__ void __launch_bounds__(kTT, 1) sv_threshold_kernel(const Params P, fl
     R.pon = pon;
     const float k = R.k;
 
-    // ---- 1: the row max, the sample and (top-p over the whole row) the row's mass ----
-    // The mass is summed against the thread's running max m (the sum rescaled when m grows).
+    // ---- 1: the sample, and for top-p over the whole row also the row max and mass ----
+    // Top-k rows read only every fourth sampled vector here (k's share needs few; the row max comes
+    // with the candidates in pass 2). Top-p rows read the whole row: the max, the sample and the
+    // mass summed against the thread's running max m (the sum rescaled when m grows).
     const bool pmass = pon && !kon;
+    const int nsamp = pmass ? nsv : (nvec + 4 * sstride - 1) / (4 * sstride);
     float mx = -INFINITY, s_run = 0.0f;
-    for (int u0 = tid; u0 < nvec; u0 += kTT * kU) {
+    if (!pmass) {
+      for (int s2 = tid; s2 < nsamp; s2 += kTT) {
+        const uint4 v = ld_pol_v4(R.rv + s2 * 4 * sstride, keep);
+        samp[s2] = v;
+        mx = max_nan(mx, vec_max<BF16>(v));
+      }
+    }
+    for (int u0 = tid; pmass && u0 < nvec; u0 += kTT * kU) {
       uint4 v[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
@@ -795,15 +870,16 @@ __global__ void __launch_bounds__(kTT, 1) sv_threshold_kernel(const Params P, fl
       sm.fm[j] = 0ull;
     }
     __syncthreads();
-    float M = -INFINITY;
+    float M = -INFINITY;                     // top-k rows: the sample's max
 #pragma unroll 8
     for (int w = 0; w < kTW; ++w) M = max_nan(M, sm.redf[w]);
-    if (!(M > -INFINITY && M < INFINITY)) {   // NaN, +inf or only -inf: the streaming kernel's row error
+    const bool m_ok = M > -INFINITY && M < INFINITY;
+    if (pmass && !m_ok) {        // NaN, +inf or only -inf: the streaming kernel's row error
       if (tid == 0) tau[r] = -INFINITY;
       __syncthreads();
       continue;
     }
-    const float Mk = M * k;
+    float Mk = M * k;
     R.Mk = Mk;
     // The row's mass relative to M, in fixed point (every thread gets it).
     unsigned long long S = 0, unused0 = 0;
@@ -814,10 +890,7 @@ __global__ void __launch_bounds__(kTT, 1) sv_threshold_kernel(const Params P, fl
     }
 
     // ---- 2: the sample's fine-bin histogram and the window ----
-    // Top-k rows take every fourth sampled vector (k's share needs few), top-p rows all of them.
-    const int sstep = pmass ? 1 : 4;
-    const int nsv_used = (nsv + sstep - 1) / sstep;
-    for (int s = tid * sstep; s < nsv; s += kTT * sstep) {
+    for (int s = tid; m_ok && s < nsamp; s += kTT) {
       const uint4 v = samp[s];
 #pragma unroll
       for (int e = 0; e < E; ++e) {
@@ -833,7 +906,7 @@ __global__ void __launch_bounds__(kTT, 1) sv_threshold_kernel(const Params P, fl
     __syncthreads();
     if (warp == 0) {
       // Logits a sampled logit stands for.
-      const float f = static_cast<float>(nvec) / static_cast<float>(nsv_used);
+      const float f = static_cast<float>(nvec) / static_cast<float>(nsamp);
       int b_t, b_c, b_lo;
       unsigned est = 0;
       unsigned before = 0, total = 0;
@@ -920,7 +993,11 @@ __global__ void __launch_bounds__(kTT, 1) sv_threshold_kernel(const Params P, fl
         sm.bi[0] = b_t;
         sm.bi[1] = b_c;
         sm.bi[2] = b_lo;
-        sm.bi[3] = static_cast<float>(est) * f <= 0.6f * kCandMax;   // the fast path
+        // The fast path; a top-k row whose sample max is not finite takes the exact path (the
+        // main pass then collects nothing).
+        const bool fast_row = m_ok && static_cast<float>(est) * f <= 0.6f * kCandMax;
+        sm.bi[3] = fast_row;
+        if (!fast_row) sm.bx[0] = sm.bx[1] = sm.bx[2] = INFINITY;
         sm.ncand = 0u;
       }
     }
@@ -930,59 +1007,75 @@ __global__ void __launch_bounds__(kTT, 1) sv_threshold_kernel(const Params P, fl
     __syncthreads();
 
     uint32_t tau_key = 0;
+    if (!pmass) {
+      // ---- 3 (top-k rows): the row max and the candidates in one pass ----
+      float m2 = -INFINITY;
+      pass2<BF16, false, true>(sm, cand, R.rv, nvec, x_t, x_t, x_t, Mk, k, first, tid, lane, m2);
+      m2 = warp_max_nan(m2);
+      if (lane == 0) sm.redf[warp] = m2;
+      __syncthreads();
+      M = -INFINITY;
+#pragma unroll 8
+      for (int w = 0; w < kTW; ++w) M = max_nan(M, sm.redf[w]);
+      if (!(M > -INFINITY && M < INFINITY)) {   // NaN, +inf or only -inf: a row error
+        if (tid == 0) tau[r] = -INFINITY;
+        __syncthreads();
+        continue;
+      }
+      Mk = M * k;
+      R.Mk = Mk;
+    }
     if (fast) {
-      // ---- 3: the mass of A (top-p), the candidates of T and C ----
-      const float s_a = pmass ? pass2<BF16, true>(sm, cand, R.rv, nvec, x_t, x_a, x_l, Mk, k, first,
-                                                  tid, lane)
-                              : pass2<BF16, false>(sm, cand, R.rv, nvec, x_t, x_t, x_t, Mk, k, first,
-                                                   tid, lane);
-      // Per-thread sums in fixed point, then block sums in warp order.
-      unsigned long long mA = pmass ? __float2ull_rn(s_a * kFix) : 0ull, unused1 = 0;
+      // ---- 3 (top-p rows): the mass of A, the candidates of T and C ----
+      unsigned long long mA = 0, unused1 = 0;
+      if (pmass) {
+        float unused_mx = 0.0f;
+        const float s_a = pass2<BF16, true, false>(sm, cand, R.rv, nvec, x_t, x_a, x_l, Mk, k,
+                                                   first, tid, lane, unused_mx);
+        mA = __float2ull_rn(s_a * kFix);       // per-thread sums in fixed point, then block sums
+      }
       block_sum2(sm, mA, unused1, lane, warp);
       const unsigned ncand = sm.ncand;
       const int nc = static_cast<int>(ncand < static_cast<unsigned>(kCandMax) ? ncand : kCandMax);
       fast = ncand <= static_cast<unsigned>(kCandMax);
 
       // ---- 4: the exact selection on the candidates ----
+      int where = 0;                             // top-p rows: the boundary in T (0) or C (1)
+      unsigned long long base = 0;
+      double target_p = 0.0;
       if (fast && kon) {
         fast = nc >= topk;                       // the k-th largest lies in the window
-        if (fast) {
-          auto all = [](float) { return true; };
-          const uint32_t kth = cand_kth<BF16>(sm, cand, nc, topk, Mk, k, all, tid, lane, warp);
-          tau_key = kth;
-          if (pon) {
-            unsigned long long km = 0, unused = 0;
-            for (int j = tid; j < nc; j += kTT) {
-              const float z = cand[j];
-              if (order_key<BF16>(z) >= kth) km += fix_mass(z, Mk, k);
-            }
-            block_sum2(sm, km, unused, lane, warp);
-            const double target = static_cast<double>(topp) * static_cast<double>(km);
-            tau_key = cand_topp<BF16>(sm, cand, nc, kth, 0ull, target, Mk, k, all, tid, lane, warp);
-          }
-        }
-      } else if (fast) {                          // top-p over the whole row
-        auto in_t = [=](float z) { return z >= x_t; };
-        auto in_c = [=](float z) { return z < x_a; };
+      } else if (fast) {                         // top-p over the whole row
         unsigned long long mT = 0, mC = 0;
         for (int j = tid; j < nc; j += kTT) {
           const float z = cand[j];
           const unsigned long long w = fix_mass(z, Mk, k);
-          if (in_t(z)) {
+          if (z >= x_t) {
             mT += w;
           } else {
             mC += w;
           }
         }
         block_sum2(sm, mT, mC, lane, warp);
-        const double target = static_cast<double>(topp) * static_cast<double>(S);
-        if (static_cast<double>(mT) >= target) {                    // the boundary lies in T
-          tau_key = cand_topp<BF16>(sm, cand, nc, 0u, 0ull, target, Mk, k, in_t, tid, lane, warp);
-        } else if (static_cast<double>(mT + mA) < target &&
-                   static_cast<double>(mT + mA + mC) >= target) {   // ... in C
-          tau_key = cand_topp<BF16>(sm, cand, nc, 0u, mT + mA, target, Mk, k, in_c, tid, lane, warp);
+        target_p = static_cast<double>(topp) * static_cast<double>(S);
+        if (static_cast<double>(mT) >= target_p) {                  // the boundary lies in T
+          where = 0;
+        } else if (static_cast<double>(mT + mA) < target_p &&
+                   static_cast<double>(mT + mA + mC) >= target_p) { // ... in C
+          where = 1;
+          base = mT + mA;
         } else {                                                     // in A, or below the window
           fast = false;
+        }
+      }
+      if (fast) {
+        if (nc <= kWarpSolve) {                  // a short list: warp 0 alone, no CTA barriers
+          if (warp == 0)
+            tau_key = cand_solve<32, BF16>(sm, cand, nc, kon, pon, topk, topp, where, base, target_p,
+                                           x_t, x_a, Mk, k, lane, lane, warp);
+        } else {
+          tau_key = cand_solve<kTT, BF16>(sm, cand, nc, kon, pon, topk, topp, where, base, target_p,
+                                          x_t, x_a, Mk, k, tid, lane, warp);
         }
       }
     }
@@ -1005,10 +1098,13 @@ cudaError_t launch_threshold(const Params& P, bool bf16, float* tau, unsigned* r
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int nrows = threshold_rows(P);
-  const int grid = nrows < sms ? nrows : sms;
+  const int grid = nrows < kCtasT * sms ? nrows : kCtasT * sms;
   const void* fn = bf16 ? reinterpret_cast<const void*>(sv_threshold_kernel<true>)
                         : reinterpret_cast<const void*>(sv_threshold_kernel<false>);
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBytesT);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   if (bf16) {
     sv_threshold_kernel<true><<<grid, kTT, kDynBytesT, stream>>>(P, tau, rows);
