@@ -47,8 +47,10 @@ constexpr float kL0PerLog2 = 4.0f;
 constexpr float kFix = 4398046511104.0f;  // 2^42: the fixed-point scale of a mass 2^-d in [0, 1]
 constexpr int kSampleVecs = 2048;         // sampled 16-byte vectors at most
 constexpr int kCandMax = 16384;           // candidate logits (fp32)
-constexpr int kU = 2;                     // vectors in flight per thread in the two passes
-constexpr int kWarpSolve = 2048;          // candidate lists up to this length: one warp selects
+#ifndef SV_THRESHOLD_UNROLL
+#define SV_THRESHOLD_UNROLL 4
+#endif
+constexpr int kU = SV_THRESHOLD_UNROLL;   // vectors in flight per thread in the two passes
 
 // Dynamic shared memory holds either the fast path's sample and candidates or the exact path's
 // per-warp level-0 histograms (never both at once).
@@ -360,52 +362,22 @@ __device__ __forceinline__ void cand_level(TShared& sm, const float* cand, int n
   group_sync<kN>();
 }
 
-// The smallest candidate key in the set (>= kmin) and the first radix shift: levels of 8 bits from
-// that key cover the set's key span (one level when it spans fewer than 256 keys).
-template <int kN, bool BF16, typename InSet>
-__device__ __forceinline__ uint32_t cand_key_range(TShared& sm, const float* cand, int nc,
-                                                   uint32_t kmin, InSet in_set, int tid, int lane,
-                                                   int warp, int& shift0) {
-  uint32_t lo = 0xffffffffu, hi = 0u;
-  for (int i = tid; i < nc; i += kN) {
-    const float z = cand[i];
-    const uint32_t key = order_key<BF16>(z);
-    if (key >= kmin && in_set(z)) {
-      lo = min(lo, key);
-      hi = max(hi, key);
-    }
-  }
-  lo = __reduce_min_sync(kFull, lo);
-  hi = __reduce_max_sync(kFull, hi);
-  if (kN != 32) {
-    if (lane == 0) {
-      sm.redu[warp] = lo;
-      sm.redm[warp] = hi;
-    }
-    __syncthreads();
-    lo = 0xffffffffu;
-    hi = 0u;
-#pragma unroll 8
-    for (int w = 0; w < kTW; ++w) {
-      lo = min(lo, sm.redu[w]);
-      hi = max(hi, static_cast<uint32_t>(sm.redm[w]));
-    }
-    __syncthreads();
-  }
-  if (lo > hi) lo = hi = kmin;                     // an empty set
-  const uint32_t span = hi - lo;
+// The first radix shift for keys in [lo, hi]: levels of 8 bits from lo cover the span (one level
+// when it spans fewer than 256 keys).
+__device__ __forceinline__ int radix_shift0(uint32_t lo, uint32_t hi) {
+  const uint32_t span = hi > lo ? hi - lo : 0u;
   const int bits = span ? 32 - __clz(span) : 0;
-  shift0 = bits <= 8 ? 0 : 8 * ((bits + 7) / 8) - 8;
-  return lo;
+  return bits <= 8 ? 0 : 8 * ((bits + 7) / 8) - 8;
 }
 
 // The k-th largest key among the candidates in the set (rank k counted from the top).
+// Every candidate key lies in [lo, hi].
 template <int kN, bool BF16, typename InSet>
-__device__ uint32_t cand_kth(TShared& sm, const float* cand, int nc, int rank, float Mk, float k,
-                             InSet in_set, int tid, int lane, int warp) {
-  int shift0 = 0;
-  uint32_t kl = cand_key_range<kN, BF16>(sm, cand, nc, 0u, in_set, tid, lane, warp, shift0);
-  for (int shift = shift0; shift >= 0; shift -= 8) {
+__device__ uint32_t cand_kth(TShared& sm, const float* cand, int nc, int rank, uint32_t lo,
+                             uint32_t hi, float Mk, float k, InSet in_set, int tid, int lane,
+                             int warp) {
+  uint32_t kl = lo;
+  for (int shift = radix_shift0(lo, hi); shift >= 0; shift -= 8) {
     cand_level<kN, BF16>(sm, cand, nc, kl, shift, 0u, false, Mk, k, in_set, tid);
     int s = 0, r2 = rank;
     if (warp == 0) {
@@ -432,15 +404,14 @@ __device__ uint32_t cand_kth(TShared& sm, const float* cand, int nc, int rank, f
 }
 
 // The smallest key (>= kmin, in the set) whose strictly-larger mass, plus `base`, stays below
-// `target`.
+// `target`. The set's keys lie in [kmin, hi].
 template <int kN, bool BF16, typename InSet>
-__device__ uint32_t cand_topp(TShared& sm, const float* cand, int nc, uint32_t kmin,
+__device__ uint32_t cand_topp(TShared& sm, const float* cand, int nc, uint32_t kmin, uint32_t hi,
                               unsigned long long base, double target, float Mk, float k,
                               InSet in_set, int tid, int lane, int warp) {
-  int shift0 = 0;
-  uint32_t kl = cand_key_range<kN, BF16>(sm, cand, nc, kmin, in_set, tid, lane, warp, shift0);
+  uint32_t kl = kmin;
   unsigned long long above = base;
-  for (int shift = shift0; shift >= 0; shift -= 8) {
+  for (int shift = radix_shift0(kmin, hi); shift >= 0; shift -= 8) {
     cand_level<kN, BF16>(sm, cand, nc, kl, shift, kmin, true, Mk, k, in_set, tid);
     int s = 0;
     unsigned long long asel = above;
@@ -471,10 +442,13 @@ __device__ uint32_t cand_topp(TShared& sm, const float* cand, int nc, uint32_t k
 template <int kN, bool BF16>
 __device__ uint32_t cand_solve(TShared& sm, const float* cand, int nc, bool kon, bool pon, int topk,
                                float topp, int where, unsigned long long base, double target_p,
-                               float x_t, float x_a, float Mk, float k, int tid, int lane, int warp) {
+                               float x_t, float x_a, float x_l, float M, float Mk, float k, int tid,
+                               int lane, int warp) {
+  const uint32_t kM = order_key<BF16>(M);                // the largest key of the row
   if (kon) {
     auto all = [](float) { return true; };
-    const uint32_t kth = cand_kth<kN, BF16>(sm, cand, nc, topk, Mk, k, all, tid, lane, warp);
+    const uint32_t kth = cand_kth<kN, BF16>(sm, cand, nc, topk, order_key<BF16>(x_t), kM, Mk, k,
+                                            all, tid, lane, warp);
     if (!pon) return kth;
     unsigned long long km = 0, unused = 0;
     for (int j = tid; j < nc; j += kN) {
@@ -483,14 +457,17 @@ __device__ uint32_t cand_solve(TShared& sm, const float* cand, int nc, bool kon,
     }
     group_sum2<kN>(sm, km, unused, lane, warp);
     const double target = static_cast<double>(topp) * static_cast<double>(km);
-    return cand_topp<kN, BF16>(sm, cand, nc, kth, 0ull, target, Mk, k, all, tid, lane, warp);
+    return cand_topp<kN, BF16>(sm, cand, nc, kth, kM, 0ull, target, Mk, k, all, tid, lane, warp);
   }
   if (where == 0) {
     auto in_t = [=](float z) { return z >= x_t; };
-    return cand_topp<kN, BF16>(sm, cand, nc, 0u, 0ull, target_p, Mk, k, in_t, tid, lane, warp);
+    return cand_topp<kN, BF16>(sm, cand, nc, order_key<BF16>(x_t), kM, 0ull, target_p, Mk, k, in_t,
+                               tid, lane, warp);
   }
   auto in_c = [=](float z) { return z < x_a; };
-  return cand_topp<kN, BF16>(sm, cand, nc, 0u, base, target_p, Mk, k, in_c, tid, lane, warp);
+  const uint32_t ka = order_key<BF16>(x_a);
+  return cand_topp<kN, BF16>(sm, cand, nc, order_key<BF16>(x_l), ka > 0u ? ka - 1u : 0u, base,
+                             target_p, Mk, k, in_c, tid, lane, warp);
 }
 
 // ---- the exact path over the whole row ----
@@ -703,14 +680,17 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, const uint4* rv
                                        int lane, float& mx) {
   constexpr int E = BF16 ? 8 : 4;
   float s_a = 0.0f;
-  for (int u0 = 0; u0 < nvec; u0 += kTT * kU) {
-    uint4 vv[kU];
+  auto load = [&](int base, uint4 (&dst)[kU]) {
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
-      const int u = u0 + j * kTT + tid;
-      vv[j] = make_uint4(0u, 0u, 0u, 0u);
-      if (u < nvec) vv[j] = ld_pol_v4(rv + u, pol);
+      const int u = base + j * kTT + tid;
+      dst[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (u < nvec) dst[j] = ld_pol_v4(rv + u, pol);
     }
+  };
+  for (int u0 = 0; u0 < nvec; u0 += kTT * kU) {
+    uint4 vv[kU];
+    load(u0, vv);
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
       const bool in = u0 + j * kTT + tid < nvec;
@@ -911,9 +891,11 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
       unsigned est = 0;
       unsigned before = 0, total = 0;
       if (kon) {
-        // Down to where the sample holds k's share plus four deviations and eight more.
+        // Down to where the sample holds k's share plus three deviations and three more (more
+        // than that many sampled logits among the top k has a chance near 1e-4; the check after
+        // pass 2 sends such a row to the exact path).
         const float ks = static_cast<float>(topk) / f;
-        const unsigned want = static_cast<unsigned>(ceilf(ks + 4.0f * sqrtf(ks) + 8.0f));
+        const unsigned want = static_cast<unsigned>(ceilf(ks + 3.0f * sqrtf(ks) + 3.0f));
         const int j = warp_first_reach<16, false, unsigned>(sm.fc, 0, want, lane, before, total);
         b_lo = j < 0 ? kFB : j;
         est = j < 0 ? total + sm.fc[kFB] : before + sm.fc[j];
@@ -1069,14 +1051,8 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
         }
       }
       if (fast) {
-        if (nc <= kWarpSolve) {                  // a short list: warp 0 alone, no CTA barriers
-          if (warp == 0)
-            tau_key = cand_solve<32, BF16>(sm, cand, nc, kon, pon, topk, topp, where, base, target_p,
-                                           x_t, x_a, Mk, k, lane, lane, warp);
-        } else {
-          tau_key = cand_solve<kTT, BF16>(sm, cand, nc, kon, pon, topk, topp, where, base, target_p,
-                                          x_t, x_a, Mk, k, tid, lane, warp);
-        }
+        tau_key = cand_solve<kTT, BF16>(sm, cand, nc, kon, pon, topk, topp, where, base, target_p,
+                                        x_t, x_a, x_l, M, Mk, k, tid, lane, warp);
       }
     }
     __syncthreads();
