@@ -61,7 +61,7 @@ constexpr int kDynBytesT = kFastBytes > kSlowBytes ? kFastBytes : kSlowBytes;
 
 struct TShared {
   unsigned fc[kFB + 1];                   // sample: fine-bin counts
-  unsigned long long fm[kFB + 1];         // sample: fine-bin masses (fixed point)
+  unsigned fd[kFB + 1];                   // sample: fine-bin sums of 2^16 (w / 2^-(b+1)/8 - 1)
   unsigned c0[kL0 + 1];                   // exact path: level-0 counts (index kL0: the tail)
   unsigned long long m0[kL0 + 1];
   unsigned rc[256];                       // a radix level
@@ -348,6 +348,9 @@ __device__ __forceinline__ void cand_level(TShared& sm, const float* cand, int n
     sm.rm[j] = 0ull;
   }
   group_sync<kN>();
+  // At the last level a sub-range is one key, and every logit of a key has the same mass: the
+  // sub-range's mass is its count times that mass (the same integer as the sum), no atomics.
+  const bool by_key = masses && shift == 0;
   const unsigned long long span = 256ull << shift;
   for (int i = tid; i < nc; i += kN) {
     const float z = cand[i];
@@ -356,10 +359,17 @@ __device__ __forceinline__ void cand_level(TShared& sm, const float* cand, int n
     if (key >= kl && off < span && key >= kmin && in_set(z)) {
       const int s = static_cast<int>(off >> shift);
       atomicAdd(&sm.rc[s], 1u);
-      if (masses) atomicAdd(&sm.rm[s], fix_mass(z, Mk, k));
+      if (masses && !by_key) atomicAdd(&sm.rm[s], fix_mass(z, Mk, k));
     }
   }
   group_sync<kN>();
+  if (by_key) {
+    for (int j = tid; j < 256; j += kN) {
+      const unsigned c = sm.rc[j];
+      if (c != 0u) sm.rm[j] = static_cast<unsigned long long>(c) * fix_mass(key_value<BF16>(kl + j), Mk, k);
+    }
+    group_sync<kN>();
+  }
 }
 
 // The first radix shift for keys in [lo, hi]: levels of 8 bits from lo cover the span (one level
@@ -847,7 +857,7 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
     if (lane == 0) sm.redf[warp] = mx;
     for (int j = tid; j <= kFB; j += kTT) {
       sm.fc[j] = 0u;
-      sm.fm[j] = 0ull;
+      sm.fd[j] = 0u;
     }
     __syncthreads();
     float M = -INFINITY;                     // top-k rows: the sample's max
@@ -877,9 +887,13 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
         const float z = vec_get<BF16>(v, e);
         const int bin = d_bin(z, Mk, k, kFBPerLog2, kFB);
         atomicAdd(&sm.fc[bin], 1u);
-        if (pmass) {
-          const float w = fminf(ex2(fmaf(z, k, -Mk)), 1.0f);
-          atomicAdd(&sm.fm[bin], __float2ull_rn(w * kFix));
+        if (pmass && bin < kFB) {
+          // A logit of bin b has w in (2^-(b+1)/8, 2^-b/8]: its mass is 2^-(b+1)/8 (1 + delta),
+          // delta in [0, 2^(1/8) - 1], summed in 16-bit fixed point (a bin of 16,384 sampled logits
+          // stays below 2^27). Native 32-bit atomics; the bin's mass is rebuilt from the two sums.
+          const float e = fmaf(z, k, -Mk) + static_cast<float>(bin + 1) / kFBPerLog2;
+          const float dlt = fminf(fmaxf(ex2(e) - 1.0f, 0.0f), 0.125f);
+          atomicAdd(&sm.fd[bin], __float2uint_rn(dlt * 65536.0f));
         }
       }
     }
@@ -910,43 +924,46 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
         // the bins >= b), with its standard deviation sqrt(f (f - 1) * sample squared mass), gives
         // est_above(b) = S - m_lo(b). A: bins < b_c, the largest b_c with est_above + 5 sd below
         // top_p * S; C ends at b_lo, the smallest with est_above(b_lo + 1) - 5 sd at or above it.
-        const float Sf = static_cast<float>(S);
+        // Masses in units of the max's: the row's S, the sample's per bin.
+        const float Sf = static_cast<float>(S) * (1.0f / kFix);
         const float target = topp * Sf;
-        const float ff32 = f;
-        // Squared masses bounded by mass times the bin's largest weight 2^(-b/8).
-        unsigned long long tmi = 0;
-        float tm2 = 0.0f;
+        auto bin_mass = [&](int bb) {
+          return ex2(-static_cast<float>(bb + 1) / kFBPerLog2) *
+                 (static_cast<float>(sm.fc[bb]) + static_cast<float>(sm.fd[bb]) * (1.0f / 65536.0f));
+        };
+        // Squared masses bounded by mass times the bin's largest weight 2^(-b/8). The tail bin's
+        // logits (w < 2^-64) add nothing.
+        float tm = 0.0f, tm2 = 0.0f;
         for (int i2 = 0; i2 < 16; ++i2) {
           const int bb = lane * 16 + i2;
-          tmi += sm.fm[bb];
-          tm2 += static_cast<float>(sm.fm[bb]) * ex2(-static_cast<float>(bb) / kFBPerLog2);
+          const float mb = bin_mass(bb);
+          tm += mb;
+          tm2 += mb * ex2(-static_cast<float>(bb) / kFBPerLog2);
         }
-        // Sample mass of the bins >= this lane's first bin: the lanes above plus the tail bin.
-        unsigned long long sfx = tmi;
-        float sfx2 = tm2;
+        // Sample mass of the bins >= this lane's first bin: the lanes above.
+        float sfx = tm, sfx2 = tm2;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const unsigned long long y = __shfl_down_sync(kFull, sfx, o);
+          const float y = __shfl_down_sync(kFull, sfx, o);
           const float y2 = __shfl_down_sync(kFull, sfx2, o);
           if (lane + o < 32) {
             sfx += y;
             sfx2 += y2;
           }
         }
-        sfx += sm.fm[kFB];
-        // Variances: f (f - 1) times the sample's squared masses (fixed point: times 2^42 more).
-        const float ffk = ff32 * (ff32 - 1.0f) * kFix;
+        // Variances: f (f - 1) times the sample's squared masses.
+        const float ffk = f * (f - 1.0f);
         int bc_l = -1, blo_l = kFB;
-        unsigned long long sb = sfx;                 // sample mass of bins >= lane * 16 + i2
-        float sb2 = sfx2;
+        float sb = sfx, sb2 = sfx2;                  // sample mass of bins >= lane * 16 + i2
         for (int i2 = 0; i2 < 16; ++i2) {
           const int bb = lane * 16 + i2;
-          const float ea = Sf - ff32 * static_cast<float>(sb);
+          const float ea = Sf - f * sb;
           const float sd = 5.0f * sqrtf(ffk * fmaxf(sb2, 0.0f));
           if (ea + sd <= target) bc_l = bb;          // A = bins < bb stays below the target
-          sb -= sm.fm[bb];
-          sb2 -= static_cast<float>(sm.fm[bb]) * ex2(-static_cast<float>(bb) / kFBPerLog2);
-          const float ea1 = Sf - ff32 * static_cast<float>(sb);
+          const float mb = bin_mass(bb);
+          sb -= mb;
+          sb2 -= mb * ex2(-static_cast<float>(bb) / kFBPerLog2);
+          const float ea1 = Sf - f * fmaxf(sb, 0.0f);
           const float sd1 = 5.0f * sqrtf(ffk * fmaxf(sb2, 0.0f));
           if (blo_l == kFB && ea1 - sd1 >= target) blo_l = bb;   // bins <= bb reach it
         }
