@@ -440,7 +440,8 @@ def run_gpu(args):
     B, G, V = w.B, w.G, w.V
     dcode = sv.SV_DTYPE_BF16 if cfg.dtype == "bf16" else sv.SV_DTYPE_F32
     stream = torch.cuda.current_stream(dev)
-    ws = sv.workspace_for(B, G, V, dcode, dev, stream)
+    # --filter: the workspace with room for the kept lists (spec_verify_filtered_workspace_size)
+    ws = sv.workspace_for(B, G, V, dcode, dev, stream, filtered=args.filter)
     out_tokens = torch.empty((B, G + 1), dtype=torch.int32, device=dev)
     out_num = torch.empty((B,), dtype=torch.int32, device=dev)
     out_alpha = torch.empty((B, G), dtype=torch.float32, device=dev)
@@ -595,13 +596,14 @@ def run_gpu(args):
                        "padded_positions_per_gpu": B * (G + 1),
                        "algorithmic_bytes_per_step": algo_bytes,
                        "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
-            # --filter: the threshold kernel, then the masked streaming kernel (two launches a
-            # step; the step's time is the roofline's)
-            "gpu_launches": args.steps * (2 if args.filter else 1),
+            # --filter: the threshold kernel, the list kernel, then the masked streaming kernel
+            # (three launches a step; the step's time is the roofline's)
+            "gpu_launches": args.steps * (3 if args.filter else 1),
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                          "frac": achieved_gbs / peak, "peak_kind": peak_kind,
                          "frac_of_8tbs": achieved_gbs / NOMINAL_HBM_GBS, "traffic": traffic,
-                         "kernel": ("sv_threshold_kernel + masked " if args.filter else "")
+                         "kernel": ("sv_threshold_kernel + sv_listed_kernel + masked "
+                                    if args.filter else "")
                          + "sv_stream_kernel" + ("<bf16>" if cfg.dtype == "bf16" else "<f32>")},
             "clocks": clock_info,
             "e2e": e2e,

@@ -202,8 +202,9 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_token
  *                   <= 0 is a row error (outputs -1 / 0). NULL: off for every row.
  * Both filters keep an upper set of the row's logits, so one threshold per row describes them: the
  * call enqueues on `cuda_stream` the threshold kernel of spec_verify_filter_thresholds (into the
- * workspace), the streaming kernel of spec_verify_ex reading every logit below its row's threshold
- * as -inf, and a memset that clears the thresholds again.
+ * workspace), with a workspace of spec_verify_filtered_workspace_size bytes the list kernel (below),
+ * the streaming kernel of spec_verify_ex reading every logit below its row's threshold as -inf (it
+ * skips the rows the list kernel verified), and a memset that clears the workspace's filter area.
  * Everything else (arguments, layout, ownership, workspace, errors) as in spec_verify_ex. Only rows
  * of 16-byte multiples are supported (else SV_ERR_BAD_SHAPE), with 16-byte aligned logit bases
  * (else SV_ERR_MISALIGNED), within the streaming kernel's row limits (bf16 V <= 1048576, fp32
@@ -215,6 +216,16 @@ int spec_verify_filtered(const void* target_logits, const void* draft_logits,
                          float* out_alpha, float* out_p_draft, float* out_q_draft,
                          int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                          void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* Workspace bytes with which spec_verify_filtered also verifies from kept lists (0 for invalid
+ * sizes): spec_verify_workspace_size(...) plus, per logit row, a count and 128 (index, logit)
+ * entries, plus a flag per batch row (about 1 KB per logit row). With a workspace this large, a
+ * sampled batch row with top-k on whose logit rows each keep at most 128 logits is verified from
+ * those lists (the threshold kernel writes them; a list kernel runs the rule on them) instead of by
+ * the streaming kernel; the outputs follow the same rule. A smaller workspace (at least
+ * spec_verify_workspace_size) runs every row on the streaming kernel. Every call leaves the whole
+ * workspace zeroed. */
+size_t spec_verify_filtered_workspace_size(int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
 
 /* The per-row thresholds of top-k / top-p filtering that spec_verify_filtered applies: for every
  * logit row the rule reads in a sampled batch row whose top_k or top_p is on, the smallest logit

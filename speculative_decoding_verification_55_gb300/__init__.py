@@ -10,6 +10,7 @@ from ._binding import (SV_DTYPE_BF16, SV_DTYPE_F32, SV_MAX_GAMMA, SV_OK, SpecVer
                        spec_verify_tree_greedy, verify_tree, spec_verify_kv_rollback,
                        spec_verify_status_string,
                        spec_verify_version, spec_verify_workspace_size,
+                       spec_verify_filtered_workspace_size,
                        spec_verify_workspace_status, verify, workspace_for,
                        spec_verify_staging_size, spec_verify_staged, spec_verify_staged_h2d_bytes,
                        verify_staged)

@@ -27,7 +27,8 @@ SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 EXPORTED = ("spec_verify", "spec_verify_ex", "spec_verify_noalloc", "spec_verify_onehot",
             "spec_verify_filtered", "spec_verify_filter_thresholds", "spec_verify_tree_greedy",
             "spec_verify_kv_rollback",
-            "spec_verify_workspace_size", "spec_verify_workspace_status", "spec_verify_status_string",
+            "spec_verify_workspace_size", "spec_verify_filtered_workspace_size",
+            "spec_verify_workspace_status", "spec_verify_status_string",
             "spec_verify_version")
 
 _lib = None
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
             L.spec_verify_kv_rollback.restype = ctypes.c_int
             L.spec_verify_workspace_size.argtypes = [i32, i32, i32, i32]
             L.spec_verify_workspace_size.restype = ctypes.c_size_t
+            L.spec_verify_filtered_workspace_size.argtypes = [i32, i32, i32, i32]
+            L.spec_verify_filtered_workspace_size.restype = ctypes.c_size_t
             L.spec_verify_workspace_status.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_int32), vp]
             L.spec_verify_workspace_status.restype = ctypes.c_int
             L.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -95,6 +98,10 @@ def lib() -> ctypes.CDLL:
 
 def spec_verify_workspace_size(B: int, gamma_max: int, V: int, dtype: int) -> int:
     return int(lib().spec_verify_workspace_size(B, gamma_max, V, dtype))
+
+
+def spec_verify_filtered_workspace_size(B: int, gamma_max: int, V: int, dtype: int) -> int:
+    return int(lib().spec_verify_filtered_workspace_size(B, gamma_max, V, dtype))
 
 
 def spec_verify_status_string(status: int) -> str:
@@ -484,11 +491,13 @@ def spec_verify(target_logits, draft_logits, draft_tokens, draft_len, temperatur
 _ws_cache = {}
 
 
-def workspace_for(B, G, V, dtype_code, device, stream=None):
-    """A zero-initialised workspace cached per (device, stream), grown on demand. Calls leave it
-    zeroed, so it is reused without clearing; it must not serve two calls in flight at once."""
+def workspace_for(B, G, V, dtype_code, device, stream=None, filtered=False):
+    """A zero-initialised workspace cached per (device, stream), grown on demand (``filtered``: the
+    size with which spec_verify_filtered also verifies from kept lists). Calls leave it zeroed, so
+    it is reused without clearing; it must not serve two calls in flight at once."""
     import torch
-    need = spec_verify_workspace_size(B, G, V, dtype_code)
+    need = (spec_verify_filtered_workspace_size if filtered else spec_verify_workspace_size)(
+        B, G, V, dtype_code)
     key = (str(device), _stream_handle(stream, device))
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < need:
@@ -512,8 +521,9 @@ def verify(target_logits, draft_logits, draft_tokens, draft_len, temperature, un
     out_alpha = torch.empty((B, G), dtype=torch.float32, device=dev)
     out_p = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
     out_q = torch.empty((B, G), dtype=torch.float32, device=dev) if with_probs else None
-    ws = workspace_for(B, G, V, _dtype_code(target_logits), dev, stream)
-    if top_k is not None or top_p is not None:
+    filtered = top_k is not None or top_p is not None
+    ws = workspace_for(B, G, V, _dtype_code(target_logits), dev, stream, filtered=filtered)
+    if filtered:
         if onehot:
             raise ValueError("filtering with one-hot drafts is not supported")
         spec_verify_filtered(target_logits, draft_logits, draft_tokens, draft_len, temperature,

@@ -10,7 +10,8 @@ from pathlib import Path
 PKG_DIR = Path(__file__).resolve().parent
 CSRC = PKG_DIR / "csrc"
 SOURCES = [CSRC / "sv_api.cu", CSRC / "sv_stream.cu", CSRC / "sv_element.cu", CSRC / "sv_noalloc.cu",
-           CSRC / "sv_rollback.cu", CSRC / "sv_threshold.cu", CSRC / "sv_staged.cu"]
+           CSRC / "sv_rollback.cu", CSRC / "sv_threshold.cu", CSRC / "sv_listed.cu",
+           CSRC / "sv_staged.cu"]
 DEPS = [CSRC / "sv_common.cuh", PKG_DIR.parent / "include" / "spec_verify.h"]
 LIB_NAME = "libspecverify.so"
 LIB_PATH = PKG_DIR / LIB_NAME

@@ -52,6 +52,18 @@ size_t thresholds_offset(int32_t B, int32_t G) {
 }
 size_t threshold_rows_of(int32_t B, int32_t G) { return static_cast<size_t>(B) * (2 * G + 1); }
 
+// Past spec_verify_workspace_size, the larger workspace of spec_verify_filtered_workspace_size
+// holds the kept lists: per threshold row a count, per batch row a "verified from its lists" flag,
+// then per threshold row kList (index, logit) entries. All of it is cleared after each call.
+constexpr size_t kListBytes = sv::kList * sizeof(int2);   // one row's kept list
+size_t list_counts_offset(int32_t B, int32_t G, int32_t V, int32_t dtype) {
+  return spec_verify_workspace_size(B, G, V, dtype);
+}
+size_t lists_offset(int32_t B, int32_t G, int32_t V, int32_t dtype) {
+  return list_counts_offset(B, G, V, dtype) +
+         align_up((threshold_rows_of(B, G) + static_cast<size_t>(B)) * sizeof(int), 256);
+}
+
 bool sizes_ok(int32_t B, int32_t G, int32_t V, int32_t dtype) {
   if (B < 1 || G < 0 || G > SV_MAX_GAMMA || V < 1) return false;
   if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return false;
@@ -409,6 +421,12 @@ int filter_args_status(const void* target_logits, const void* draft_logits, cons
 
 extern "C" {
 
+size_t spec_verify_filtered_workspace_size(int32_t B, int32_t gamma_max, int32_t V, int32_t dtype) {
+  if (!sizes_ok(B, gamma_max, V, dtype)) return 0;
+  return lists_offset(B, gamma_max, V, dtype) +
+         align_up(threshold_rows_of(B, gamma_max) * kListBytes, 256);
+}
+
 int spec_verify_filter_thresholds(const void* target_logits, const void* draft_logits,
                                   const int32_t* draft_len, const float* temperature,
                                   const int32_t* top_k, const float* top_p, float* out_thresholds,
@@ -434,7 +452,7 @@ int spec_verify_filter_thresholds(const void* target_logits, const void* draft_l
   P.B = B;
   P.G = G;
   P.V = V;
-  if (sv::launch_threshold(P, dtype == SV_DTYPE_BF16, out_thresholds, nullptr,
+  if (sv::launch_threshold(P, dtype == SV_DTYPE_BF16, out_thresholds, nullptr, nullptr, nullptr,
                            static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
     return SV_ERR_CUDA;
   return SV_OK;
@@ -492,8 +510,21 @@ int spec_verify_filtered(const void* target_logits, const void* draft_logits,
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
   // 1. The threshold of every row a filter touches (-inf for the others).
   unsigned* row_counter = reinterpret_cast<unsigned*>(tau + threshold_rows_of(B, G));
-  if (sv::launch_threshold(P, bf16, tau, row_counter, stream) != cudaSuccess) return SV_ERR_CUDA;
-  // 2. The streaming kernel with every logit below its row's threshold read as -inf.
+  // A workspace of spec_verify_filtered_workspace_size bytes also takes the kept lists.
+  const size_t need_lists = spec_verify_filtered_workspace_size(B, G, V, dtype);
+  const bool with_lists = workspace_bytes >= need_lists;
+  int* list_n = with_lists ? reinterpret_cast<int*>(ws + list_counts_offset(B, G, V, dtype)) : nullptr;
+  int* listed = with_lists ? list_n + threshold_rows_of(B, G) : nullptr;
+  int2* lists = with_lists ? reinterpret_cast<int2*>(ws + lists_offset(B, G, V, dtype)) : nullptr;
+  if (sv::launch_threshold(P, bf16, tau, row_counter, lists, list_n, stream) != cudaSuccess)
+    return SV_ERR_CUDA;
+  // 2. Batch rows whose logit rows all have kept lists: verified from the lists.
+  if (with_lists) {
+    if (sv::launch_listed(P, lists, list_n, listed, stream) != cudaSuccess) return SV_ERR_CUDA;
+    P.listed = listed;
+  }
+  // 3. The streaming kernel (the other rows) with every logit below its row's threshold read as
+  //    -inf.
   P.tau = tau;
   const long long slots = static_cast<long long>(B) * (G + 1);
   P.units = static_cast<int>(row_bytes / 16);
@@ -503,10 +534,10 @@ int spec_verify_filtered(const void* target_logits, const void* draft_logits,
   if (max_clusters(dev, bf16, P.C, &maxc, true) != SV_OK) return SV_ERR_CUDA;
   P.nclusters = static_cast<int>(slots < maxc ? slots : maxc);
   if (sv::launch_stream(P, bf16, stream) != cudaSuccess) return SV_ERR_CUDA;
-  // 3. Leave the workspace zeroed: a later call of other sizes keeps its counters where these
-  //    thresholds and the row counter were.
-  if (cudaMemsetAsync(tau, 0, need - thresholds_offset(B, G), stream) != cudaSuccess)
-    return SV_ERR_CUDA;
+  // 4. Leave the workspace zeroed: a later call of other sizes keeps its counters where these
+  //    thresholds, the row counter and the lists were.
+  const size_t used = (with_lists ? need_lists : need) - thresholds_offset(B, G);
+  if (cudaMemsetAsync(tau, 0, used, stream) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }
 

@@ -75,9 +75,14 @@ struct Params {
   // Filtered verification by thresholds: per row the smallest logit the filters keep (target rows
   // [B, G+1], then draft rows [B, G]); the streaming kernel reads every logit below it as -inf.
   const float* tau;
+  // Filtered batch rows already verified from their kept lists (nonzero: the streaming kernel
+  // leaves the row alone), or null.
+  const int* listed;
 };
 
 constexpr int kMaxTreeNodes = 65;    // N <= SV_MAX_GAMMA + 1
+// Kept lists of filtered logit rows: at most kList (index, logit) entries per row.
+constexpr int kList = 128;
 
 // ------------------------------------------------------------------------------------------------
 // Arithmetic
@@ -612,6 +617,11 @@ __device__ __forceinline__ Pos classify(const Params& P, int s) {
   p.load = p.len_ok && p.t_ok && p.i <= p.gb;
   p.two = p.load && !p.greedy && p.i < p.gb && !P.onehot;
   p.oh = p.load && !p.greedy && p.i < p.gb && P.onehot;
+  if (kMask && P.listed && __ldg(P.listed + p.b) != 0) {   // verified from its kept lists
+    p.len_ok = p.t_ok = true;
+    p.load = p.two = p.oh = false;
+    return p;
+  }
   if (kMask && !p.greedy && P.top_p) {
     const float pp = __ldg(P.top_p + p.b);
     if (!(pp > 0.0f)) {                        // NaN fails too
@@ -958,7 +968,13 @@ cudaError_t stream_max_clusters(bool bf16, bool wide, int C, int* n, bool masked
 // rows [B, G+1] then draft rows [B, G]. rows: a zeroed device counter the CTAs claim rows from (it
 // ends at rows + grid size), or null for a static split.
 int threshold_rows(const Params& P);
-cudaError_t launch_threshold(const Params& P, bool bf16, float* tau, unsigned* rows,
-                             cudaStream_t stream);
+// lists / list_n (or null): per threshold row, kList (index, logit bits) entries and their count;
+// a top-k row solved on its candidate list writes its kept set there when it fits, the other rows
+// leave list_n at 0.
+cudaError_t launch_threshold(const Params& P, bool bf16, float* tau, unsigned* rows, int2* lists,
+                             int* list_n, cudaStream_t stream);
+// Verifies the filtered batch rows whose logit rows all have kept lists, and marks them in listed.
+cudaError_t launch_listed(const Params& P, const int2* lists, const int* list_n, int* listed,
+                          cudaStream_t stream);
 
 }  // namespace sv

@@ -47,6 +47,7 @@ constexpr float kL0PerLog2 = 4.0f;
 constexpr float kFix = 4398046511104.0f;  // 2^42: the fixed-point scale of a mass 2^-d in [0, 1]
 constexpr int kSampleVecs = 2048;         // sampled 16-byte vectors at most
 constexpr int kCandMax = 16384;           // candidate logits (fp32)
+constexpr int kIdxMax = kSampleVecs * 4;  // candidate indices kept (in the sample's place)
 #ifndef SV_THRESHOLD_UNROLL
 #define SV_THRESHOLD_UNROLL 4
 #endif
@@ -683,11 +684,12 @@ __device__ __noinline__ uint32_t exact_row(TShared& sm, unsigned char* dyn, cons
 // Pass 2 over the row: candidates (cut points of class_words) appended to `cand` in shared memory
 // (warp-aggregated: one atomic per warp and vector step with a candidate), and (kP) the thread's
 // fp32 sum of the masses between the cut points; kMax: also the thread's max (NaN-propagating) in
-// mx. Every thread calls it with the same trip count.
+// mx; cidx (or null): each candidate's logit index, for the first kIdxMax candidates. Every thread
+// calls it with the same trip count.
 template <bool BF16, bool kP, bool kMax>
-__device__ __forceinline__ float pass2(TShared& sm, float* cand, const uint4* rv, int nvec, float xt,
-                                       float xa, float xl, float Mk, float k, uint64_t pol, int tid,
-                                       int lane, float& mx) {
+__device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, const uint4* rv,
+                                       int nvec, float xt, float xa, float xl, float Mk, float k,
+                                       uint64_t pol, int tid, int lane, float& mx) {
   constexpr int E = BF16 ? 8 : 4;
   float s_a = 0.0f;
   auto load = [&](int base, uint4 (&dst)[kU]) {
@@ -732,10 +734,12 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, const uint4* rv
         if (lane == 31) pos0 = atomicAdd(&sm.ncand, static_cast<unsigned>(incl));
         pos0 = __shfl_sync(kFull, pos0, 31);
         unsigned pos = pos0 + static_cast<unsigned>(incl - c);
+        const int ubase = (u0 + j * kTT + tid) * E;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           if ((cm >> e) & 1u) {
             if (pos < static_cast<unsigned>(kCandMax)) cand[pos] = vec_get<BF16>(v, e);
+            if (cidx != nullptr && pos < static_cast<unsigned>(kIdxMax)) cidx[pos] = ubase + e;
             ++pos;
           }
         }
@@ -747,9 +751,11 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, const uint4* rv
 
 // rows: null, or a zeroed counter from which CTAs claim rows one at a time (rows differ in cost by
 // a few times); without it, CTA c takes rows c, c + gridDim.x, ...
+// lists / list_n: see launch_threshold.
 template <bool BF16>
 __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params P, float* tau,
-                                                              unsigned* rows) {
+                                                              unsigned* rows, int2* lists,
+                                                              int* list_n) {
   __shared__ TShared sm;
   extern __shared__ __align__(16) unsigned char dyn_t[];
   uint4* samp = reinterpret_cast<uint4*>(dyn_t);
@@ -1009,7 +1015,8 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
     if (!pmass) {
       // ---- 3 (top-k rows): the row max and the candidates in one pass ----
       float m2 = -INFINITY;
-      pass2<BF16, false, true>(sm, cand, R.rv, nvec, x_t, x_t, x_t, Mk, k, first, tid, lane, m2);
+      pass2<BF16, false, true>(sm, cand, lists ? reinterpret_cast<int*>(samp) : nullptr, R.rv,
+                               nvec, x_t, x_t, x_t, Mk, k, first, tid, lane, m2);
       m2 = warp_max_nan(m2);
       if (lane == 0) sm.redf[warp] = m2;
       __syncthreads();
@@ -1029,8 +1036,8 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
       unsigned long long mA = 0, unused1 = 0;
       if (pmass) {
         float unused_mx = 0.0f;
-        const float s_a = pass2<BF16, true, false>(sm, cand, R.rv, nvec, x_t, x_a, x_l, Mk, k,
-                                                   first, tid, lane, unused_mx);
+        const float s_a = pass2<BF16, true, false>(sm, cand, nullptr, R.rv, nvec, x_t, x_a, x_l,
+                                                   Mk, k, first, tid, lane, unused_mx);
         mA = __float2ull_rn(s_a * kFix);       // per-thread sums in fixed point, then block sums
       }
       block_sum2(sm, mA, unused1, lane, warp);
@@ -1071,6 +1078,30 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
         tau_key = cand_solve<kTT, BF16>(sm, cand, nc, kon, pon, topk, topp, where, base, target_p,
                                         x_t, x_a, x_l, M, Mk, k, tid, lane, warp);
       }
+      // ---- 5 (top-k rows): the kept set, when it is short, as an (index, logit) list ----
+      if (fast && kon && lists != nullptr && nc <= kIdxMax) {
+        const int* cidx = reinterpret_cast<const int*>(samp);
+        unsigned nk = 0;
+        for (int j = tid; j < nc; j += kTT) nk += order_key<BF16>(cand[j]) >= tau_key ? 1u : 0u;
+        nk = __reduce_add_sync(kFull, nk);
+        if (lane == 0) sm.redu[warp] = nk;
+        if (tid == 0) sm.ncand = 0u;             // reused as the list's fill counter
+        __syncthreads();
+        nk = 0;
+#pragma unroll 8
+        for (int w = 0; w < kTW; ++w) nk += sm.redu[w];
+        if (nk <= static_cast<unsigned>(kList)) {
+          int2* out = lists + static_cast<size_t>(r) * kList;
+          for (int j = tid; j < nc; j += kTT) {
+            const float z = cand[j];
+            if (order_key<BF16>(z) >= tau_key) {
+              const unsigned pos = atomicAdd(&sm.ncand, 1u);
+              out[pos] = make_int2(cidx[j], __float_as_int(z));
+            }
+          }
+          if (tid == 0) list_n[r] = static_cast<int>(nk);
+        }
+      }
     }
     __syncthreads();
     if (!fast) tau_key = exact_row<BF16>(sm, dyn_t, R, tid, lane, warp);
@@ -1083,8 +1114,8 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
 
 int threshold_rows(const Params& P) { return P.B * (2 * P.G + 1); }
 
-cudaError_t launch_threshold(const Params& P, bool bf16, float* tau, unsigned* rows,
-                             cudaStream_t stream) {
+cudaError_t launch_threshold(const Params& P, bool bf16, float* tau, unsigned* rows, int2* lists,
+                             int* list_n, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1100,9 +1131,9 @@ cudaError_t launch_threshold(const Params& P, bool bf16, float* tau, unsigned* r
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   if (bf16) {
-    sv_threshold_kernel<true><<<grid, kTT, kDynBytesT, stream>>>(P, tau, rows);
+    sv_threshold_kernel<true><<<grid, kTT, kDynBytesT, stream>>>(P, tau, rows, lists, list_n);
   } else {
-    sv_threshold_kernel<false><<<grid, kTT, kDynBytesT, stream>>>(P, tau, rows);
+    sv_threshold_kernel<false><<<grid, kTT, kDynBytesT, stream>>>(P, tau, rows, lists, list_n);
   }
   return cudaGetLastError();
 }

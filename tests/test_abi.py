@@ -52,6 +52,11 @@ def test_workspace_size(L):
     for B, G in ((1, 0), (1, 4), (8, 4), (1024, 8), (7, 64)):
         n = m.spec_verify_workspace_size(B, G, 32000, 1)
         assert n % 256 == 0 and n >= 8 * B * (G + 1) + 4 * B
+    for B, G in ((1, 0), (8, 4), (1024, 8)):
+        n = m.spec_verify_workspace_size(B, G, 32000, 1)
+        f = m.spec_verify_filtered_workspace_size(B, G, 32000, 1)
+        assert f % 256 == 0 and f >= n + 128 * 8 * B * (2 * G + 1)
+    assert m.spec_verify_filtered_workspace_size(0, 4, 100, 0) == 0
     assert m.spec_verify_workspace_size(0, 4, 100, 0) == 0
     assert m.spec_verify_workspace_size(2, 65, 100, 0) == 0
     assert m.spec_verify_workspace_size(2, -1, 100, 0) == 0

@@ -430,9 +430,13 @@ def test_gpu_filtered_workspace_reused_across_sizes(sv):
     (its thresholds lie where another size keeps records and counters), so the next call of other
     sizes on the same workspace still verifies correctly."""
     dtc = sv.SV_DTYPE_F32
-    big = sv.spec_verify_workspace_size(64, 8, 4096, dtc)
-    ws = torch.zeros(big, dtype=torch.uint8, device="cuda")
-    for (B, G, V, seed) in ((4, 3, 4096, 1), (12, 3, 4096, 2), (3, 8, 4096, 3), (16, 2, 4096, 4)):
+    shapes = ((4, 3, 4096, 1), (12, 3, 4096, 2), (3, 8, 4096, 3), (16, 2, 4096, 4))
+    # Too small for the kept lists (every row on the streaming kernel), then large enough for them.
+    small = sv.spec_verify_workspace_size(64, 8, 4096, dtc)
+    assert small < min(sv.spec_verify_filtered_workspace_size(B, G, V, dtc) for B, G, V, _ in shapes)
+    large = max(sv.spec_verify_filtered_workspace_size(B, G, V, dtc) for B, G, V, _ in shapes)
+    for nbytes, (B, G, V, seed) in [(n, sh) for n in (small, large) for sh in shapes]:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda") if seed == 1 else ws
         zt, zd, x, n, T, u, top_k, top_p = filter_batch(B, G, V, "f32", seed=seed)
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()   # noqa: E731
         outs = (torch.full((B, G + 1), -7, dtype=torch.int32, device="cuda"),
