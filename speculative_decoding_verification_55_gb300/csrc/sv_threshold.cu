@@ -700,9 +700,11 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
       if (u < nvec) dst[j] = ld_pol_v4(rv + u, pol);
     }
   };
+  static_assert(kU * E <= 32, "one bit per logit of a step in a word");
   for (int u0 = 0; u0 < nvec; u0 += kTT * kU) {
     uint4 vv[kU];
     load(u0, vv);
+    unsigned bits = 0;                              // bit j*E + e: logit e of vector j is a candidate
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
       const bool in = u0 + j * kTT + tid < nvec;
@@ -710,7 +712,7 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
       uint32_t cw[4], aw[4];
       if (kMax && in) mx = max_nan(mx, vec_max<BF16>(v));
       class_words<BF16, kP>(v, xt, xa, xl, cw, aw);
-      const bool c_any = in && ((cw[0] | cw[1] | cw[2] | cw[3]) != 0u);
+      if (in && (cw[0] | cw[1] | cw[2] | cw[3]) != 0u) bits |= word_bits<BF16>(cw) << (j * E);
       if (kP && in && (aw[0] | aw[1] | aw[2] | aw[3]) != 0u) {
         const unsigned am = word_bits<BF16>(aw);
         float sa = 0.0f;
@@ -721,27 +723,29 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
         }
         s_a += sa;
       }
-      if (__any_sync(kFull, c_any)) {                  // append to the candidate list
-        const unsigned cm = c_any ? word_bits<BF16>(cw) : 0u;
-        const int c = __popc(cm);
-        int incl = c;
+    }
+    if (__any_sync(kFull, bits != 0u)) {            // append the step's candidates, once a warp
+      const int c = __popc(bits);
+      int incl = c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(kFull, incl, o);
-          if (lane >= o) incl += y;
-        }
-        unsigned pos0 = 0;
-        if (lane == 31) pos0 = atomicAdd(&sm.ncand, static_cast<unsigned>(incl));
-        pos0 = __shfl_sync(kFull, pos0, 31);
-        unsigned pos = pos0 + static_cast<unsigned>(incl - c);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      unsigned pos0 = 0;
+      if (lane == 31) pos0 = atomicAdd(&sm.ncand, static_cast<unsigned>(incl));
+      pos0 = __shfl_sync(kFull, pos0, 31);
+      unsigned pos = pos0 + static_cast<unsigned>(incl - c);
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        unsigned bj = (bits >> (j * E)) & ((1u << E) - 1u);
         const int ubase = (u0 + j * kTT + tid) * E;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          if ((cm >> e) & 1u) {
-            if (pos < static_cast<unsigned>(kCandMax)) cand[pos] = vec_get<BF16>(v, e);
-            if (cidx != nullptr && pos < static_cast<unsigned>(kIdxMax)) cidx[pos] = ubase + e;
-            ++pos;
-          }
+        while (bj != 0u) {
+          const int e = __ffs(bj) - 1;
+          bj &= bj - 1u;
+          if (pos < static_cast<unsigned>(kCandMax)) cand[pos] = vec_get<BF16>(vv[j], e);
+          if (cidx != nullptr && pos < static_cast<unsigned>(kIdxMax)) cidx[pos] = ubase + e;
+          ++pos;
         }
       }
     }
