@@ -558,7 +558,22 @@ def run_gpu(args):
         e2e = {"value": positions_all / (ms_e2e * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
                "ms_per_step": ms_e2e, "steps": n_e2e, "path": e2e_path}
-        del host, dev_in
+        # The host link's own rate, a plain page-locked copy of 1 GiB (median of 3), and the floor it
+        # sets for this step's host-to-device bytes.
+        link_h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+        link_d = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+        link_ms = []
+        for _ in range(4):
+            a, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            link_d.copy_(link_h, non_blocking=True)
+            b2.record(stream)
+            torch.cuda.synchronize(dev)
+            link_ms.append(a.elapsed_time(b2))
+        link_gbs = (1 << 30) / (sorted(link_ms[1:])[1] * 1e-3) / 1e9
+        e2e["host_link_gbs"] = link_gbs
+        e2e["host_link_floor_ms"] = bi / (link_gbs * 1e9) * 1e3
+        del host, dev_in, link_h, link_d
 
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -309,12 +309,17 @@ int spec_verify_noalloc(const void* target_logits, const void* draft_logits,
  *
  * The rule reads target rows 0..gamma_b of row b and, for a sampled row (temperature not exactly
  * 0), draft rows 0..gamma_b - 1 ([R] "Speculative decoding", rayaq.ca ml-models -- Mechanics, One
- * round, steps 3-5; The greedy case: a greedy row compares with the target's argmax only). So the
- * call enqueues on `cuda_stream`, in this order: host-to-device copies of draft_tokens, draft_len,
- * temperature and uniforms; one copy per run of contiguous logit rows that the rule reads (runs of
- * consecutive rows b merge when row b has gamma_b = gamma_max); spec_verify_ex on the staged copies
- * (p and q of the drafts are not returned); device-to-host copies of out_tokens, out_num_emitted and
- * out_alpha. Padding rows are never copied, and never read by the kernels.
+ * round, steps 3-5; The greedy case: a greedy row compares with the target's argmax only). The
+ * call enqueues on `cuda_stream` the host-to-device copies of draft_tokens, draft_len, temperature
+ * and uniforms. The batch rows then go in up to four groups of at least 64 rows: the logit rows a
+ * group's rule reads cross the host link on an internal stream of the library (one per device,
+ * created on first use): a gather kernel reading page-locked, mapped host memory directly, else
+ * one copy per run of contiguous rows (runs of consecutive rows b merge when row b has gamma_b =
+ * gamma_max). After a group's rows (an event orders it) spec_verify_ex verifies that group on
+ * `cuda_stream` while the next group's rows cross; p and q of the drafts are not returned. Last,
+ * device-to-host copies of out_tokens, out_num_emitted and out_alpha on `cuda_stream`. Everything
+ * the call enqueues is complete once `cuda_stream` is. Padding rows are never copied, and never
+ * read by the kernels.
  *
  * h_*: host buffers in the layouts of spec_verify_ex (h_draft_len may be NULL = all gamma_max;
  * h_out_alpha may be NULL; with gamma_max = 0, h_draft_logits and h_draft_tokens may be NULL). The call reads h_draft_len and

@@ -220,7 +220,7 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
                 float* out_p_draft, float* out_q_draft,
                 int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
                 void* workspace, size_t workspace_bytes, void* cuda_stream, bool onehot,
-                bool check_only = false) {
+                bool check_only = false, long long plan_slots = 0) {
   if (dtype != SV_DTYPE_F32 && dtype != SV_DTYPE_BF16) return SV_ERR_BAD_DTYPE;
   if (!sizes_ok(B, gamma_max, V, dtype)) return SV_ERR_BAD_SHAPE;
   const int G = gamma_max;
@@ -279,8 +279,10 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
     const int E = static_cast<int>(16 / es);
     const long long slots = static_cast<long long>(B) * (G + 1);
     P.units = V / E;
-    P.C = stream_plan_C(dev, bf16, static_cast<long long>(V) * static_cast<long long>(es), slots, sC,
-                        onehot);
+    // plan_slots: plan the chunks as for a batch of that many slots (the staged call verifies row
+    // groups with the whole batch's plan, so every row gets the same arithmetic as in one call).
+    P.C = stream_plan_C(dev, bf16, static_cast<long long>(V) * static_cast<long long>(es),
+                        plan_slots > 0 ? plan_slots : slots, sC, onehot);
     P.per = (P.units + P.C - 1) / P.C;
     int maxc = 0;
     if (max_clusters(dev, bf16, P.C, &maxc, false, onehot) != SV_OK) return SV_ERR_CUDA;
@@ -308,6 +310,18 @@ int verify_args_status(const void* target_logits, const void* draft_logits,
   return verify_impl(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
                      out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft, B, gamma_max,
                      V, dtype, nullptr, 0, nullptr, false, true);
+}
+
+int verify_ex_planned(const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, const int32_t* draft_len,
+                      const float* temperature, const float* uniforms, int32_t* out_tokens,
+                      int32_t* out_num_emitted, float* out_alpha, float* out_p_draft,
+                      float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream,
+                      long long plan_slots) {
+  return verify_impl(target_logits, draft_logits, draft_tokens, draft_len, temperature, uniforms,
+                     out_tokens, out_num_emitted, out_alpha, out_p_draft, out_q_draft, B, gamma_max,
+                     V, dtype, workspace, workspace_bytes, cuda_stream, false, false, plan_slots);
 }
 
 }  // namespace sv

@@ -957,6 +957,16 @@ int verify_args_status(const void* target_logits, const void* draft_logits,
                        int32_t* out_num_emitted, float* out_alpha, float* out_p_draft,
                        float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype);
 
+// spec_verify_ex with the streaming path's chunks planned as for a batch of plan_slots position
+// slots (0: this batch's own).
+int verify_ex_planned(const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, const int32_t* draft_len,
+                      const float* temperature, const float* uniforms, int32_t* out_tokens,
+                      int32_t* out_num_emitted, float* out_alpha, float* out_p_draft,
+                      float* out_q_draft, int32_t B, int32_t gamma_max, int32_t V, int32_t dtype,
+                      void* workspace, size_t workspace_bytes, void* cuda_stream,
+                      long long plan_slots);
+
 // Element path (any alignment, V <= 16 * 512 * 32): one cluster per position slot.
 cudaError_t launch_element(const Params& P, bool bf16, int vpt_index, cudaStream_t stream);
 // Streaming path (16-byte aligned rows): persistent clusters fed by bulk copies.
