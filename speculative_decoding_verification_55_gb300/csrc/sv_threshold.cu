@@ -13,24 +13,33 @@
 // kernel then verifies the batch with every logit below its row's threshold read as -inf: the
 // softmax of the kept logits is the renormalised filtered distribution.
 //
-// One CTA of 512 threads per row at a time (persistent over the rows, two CTAs per SM, so that one
-// streams while the other selects); nothing is shared between CTAs. Masses are w = 2^-d with d = (M - z) log2(e) / T the logit's log2
-// probability below the row max M. Per row:
-//   1  one pass over the row: M, and a strided sample of the row's vectors kept in shared memory.
-//   2  the sample's histogram over fine bins of d (8 per unit over [0, 64), then a tail bin) gives
-//      a window of bins that holds the boundary with a wide margin: for top-k the bins down to
-//      where the sample counts k's share plus a few deviations; for top-p the top bins (T), then
-//      bins counted as a whole (A), then the bins around top_p's share of the sample's mass (C).
-//   3  a second pass (from L2): the row's mass, the count and mass of A, and every logit of T and
-//      C copied into a shared-memory candidate list; no per-logit atomics.
-//   4  the exact selection on the candidates by radix levels of 8 bits over the logits' order keys
-//      (counts for top-k, 42-bit fixed-point masses for top-p; integer sums, the same result for
-//      any order of the atomics), after checking that the boundary does lie in the window.
+// One CTA of 512 threads per row at a time (persistent, two CTAs per SM so that one streams while
+// the other selects; rows claimed from a counter when one is given); nothing is shared between
+// CTAs. Masses are w = 2^-d with d = (M - z) log2(e) / T, the logit's log2 probability below the
+// row max M. Per row:
+//   1  top-k rows: a strided sample of 1/64 of the row's 16-byte vectors. Top-p rows (top-k off):
+//      one pass over the row for M, a 1/16 sample and the row's mass (summed against each thread's
+//      running max).
+//   2  the sample's histogram over fine bins of d (8 per unit over [0, 64), then a tail bin; top-k
+//      rows measure d from the sample's max) gives value cut points that hold the boundary with a
+//      wide margin: top-k, the logits above the bin where the sample holds k's share plus three
+//      deviations; top-p, the top bins (T), the bins counted as a whole (A) and the bins around
+//      where the mass below, estimated from the sample's tail with a five-sigma margin, reaches
+//      (1 - top_p) of the row's mass (C).
+//   3  one pass (top-k: from DRAM, also the row max; top-p: the second pass, mostly from L2):
+//      packed compares against the cut points, the logits of T and C appended to a shared-memory
+//      list (one warp-aggregated atomic per four-vector step), A's mass summed per thread.
+//   4  the exact selection on the list by radix levels of 8 bits over the logits' order keys from
+//      the list's known key range (counts for top-k, 42-bit fixed-point masses for top-p; integer
+//      sums, the same result for any order of the atomics), after checking that the boundary does
+//      lie in the window.
+//   5  with list outputs given: a top-k row's kept set, when it holds at most kList logits, as an
+//      (index, logit) list for the list kernel.
 // A row whose window misses the boundary or whose candidates do not fit (a large k, an unusual
 // sample) takes the exact path instead: level-0 histograms of counts and masses over the whole
 // row in coarse bins of d, then the same radix levels over the row (several passes, each exact).
-// Within a bin, decisions are on exact keys and integer masses; bins only partition the logits
-// (membership is recomputed with the same arithmetic in every pass).
+// Within a bin, decisions are on exact keys and integer masses; bins and cut points only choose
+// what is listed (membership is recomputed with the same compares in every pass).
 
 #include "sv_common.cuh"
 
