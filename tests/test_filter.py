@@ -450,6 +450,29 @@ def test_gpu_filtered_workspace_reused_across_sizes(sv):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gpu_filtered_bonus_only(sv, dtype):
+    """gamma_max = 0: every row is a bonus draw from its filtered target row; top-k rows go through
+    the kept lists, the others through the streaming kernel; both against the oracle."""
+    B, G, V = 8, 0, 4096
+    rng = np.random.default_rng(31)
+    zt = (rng.standard_normal((B, 1, V)) * 2.0).astype(np.float32)
+    if dtype == "bf16":
+        zt = bf16_round(zt)
+    zd = np.zeros((B, 0, V), np.float32)
+    x = np.zeros((B, 0), np.int32)
+    n = np.zeros(B, np.int32)
+    T = np.ones(B, np.float32)
+    T[7] = 0.0                                    # a greedy row
+    top_k = np.array([5, 50, 0, 0, 1, 200, 5, 5], np.int32)
+    top_p = np.array([1.0, 0.9, 0.9, 1.0, 1.0, 1.0, 1e-3, 0.5], np.float32)
+    u = rng.random((B, 2), dtype=np.float32)
+    gpu = run_filtered(sv, zt, zd, x, n, T, u, top_k, top_p, dtype)
+    check_filtered(zt, zd, x, n, T, u, top_k, top_p, gpu)
+    assert (gpu[1] == 1).all()
+
+
+@pytest.mark.gpu
 def test_gpu_filtered_row_errors(sv):
     B, G, V = 6, 2, 2048
     zt, zd, x, n, T, u, top_k, top_p = filter_batch(B, G, V, "f32", seed=8, greedy_frac=0.0)
