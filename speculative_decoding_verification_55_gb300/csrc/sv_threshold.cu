@@ -710,6 +710,7 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
     }
   };
   static_assert(kU * E <= 32, "one bit per logit of a step in a word");
+  const f32x2 k2 = pk(k, k), c2 = pk(-Mk, -Mk);
   for (int u0 = 0; u0 < nvec; u0 += kTT * kU) {
     uint4 vv[kU];
     load(u0, vv);
@@ -723,14 +724,27 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
       class_words<BF16, kP>(v, xt, xa, xl, cw, aw);
       if (in && (cw[0] | cw[1] | cw[2] | cw[3]) != 0u) bits |= word_bits<BF16>(cw) << (j * E);
       if (kP && in && (aw[0] | aw[1] | aw[2] | aw[3]) != 0u) {
-        const unsigned am = word_bits<BF16>(aw);
-        float sa = 0.0f;
+        // Two logits per packed step; a logit outside A adds zero.
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        f32x2 sa = pk(0.0f, 0.0f);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float w = ex2(fmaf(vec_get<BF16>(v, e), k, -Mk));
-          sa += ((am >> e) & 1u) ? w : 0.0f;
+        for (int q = 0; q < 4; q += BF16 ? 1 : 2) {
+          float a0, a1;
+          bool in0, in1;
+          if (BF16) {
+            upk(fma2(pk(bf_lo(w[q]), bf_hi(w[q])), k2, c2), a0, a1);
+            in0 = (aw[q] & 0xffffu) != 0u;
+            in1 = (aw[q] >> 16) != 0u;
+          } else {
+            upk(fma2(pk(__uint_as_float(w[q]), __uint_as_float(w[q + 1])), k2, c2), a0, a1);
+            in0 = aw[q] != 0u;
+            in1 = aw[q + 1] != 0u;
+          }
+          sa = add2(sa, pk(in0 ? ex2(a0) : 0.0f, in1 ? ex2(a1) : 0.0f));
         }
-        s_a += sa;
+        float s0, s1;
+        upk(sa, s0, s1);
+        s_a += s0 + s1;
       }
     }
     if (__any_sync(kFull, bits != 0u)) {            // append the step's candidates, once a warp
@@ -830,10 +844,12 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
     // ---- 1: the sample, and for top-p over the whole row also the row max and mass ----
     // Top-k rows read only every fourth sampled vector here (k's share needs few; the row max comes
     // with the candidates in pass 2). Top-p rows read the whole row: the max, the sample and the
-    // mass summed against the thread's running max m (the sum rescaled when m grows).
+    // mass, summed kU vectors at a time against the thread's running max m_run (the sum rescaled
+    // when m_run grows; packed pairs, as in the streaming kernel's pass 1).
     const bool pmass = pon && !kon;
     const int nsamp = pmass ? nsv : (nvec + 4 * sstride - 1) / (4 * sstride);
-    float mx = -INFINITY, s_run = 0.0f;
+    float mx = -INFINITY, m_run = -INFINITY;
+    f32x2 s_run = pk(0.0f, 0.0f);
     if (!pmass) {
       for (int s2 = tid; s2 < nsamp; s2 += kTT) {
         const uint4 v = ld_pol_v4(R.rv + s2 * 4 * sstride, keep);
@@ -842,36 +858,20 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
       }
     }
     for (int u0 = tid; pmass && u0 < nvec; u0 += kTT * kU) {
+      constexpr uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
       uint4 v[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int u = u0 + j * kTT;
-        if (u < nvec) v[j] = ld_pol_v4(R.rv + u, keep);
+        v[j] = u < nvec ? ld_pol_v4(R.rv + u, keep) : make_uint4(ninf, ninf, ninf, ninf);
       }
+      online_update_batch<BF16, kU>(v, k, m_run, s_run, mx);
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int u = u0 + j * kTT;
-        if (u < nvec) {
-          const float vm = vec_max<BF16>(v[j]);
-          if (pmass) {
-            if (vm > mx) {
-              s_run *= ex2((mx - vm) * k);
-              mx = vm;
-            }
-            if (mx > -INFINITY) {
-              const float mk = mx * k;
-              float sv = 0.0f;
-#pragma unroll
-              for (int e = 0; e < E; ++e) sv += ex2(fmaf(vec_get<BF16>(v[j], e), k, -mk));
-              s_run += sv;
-            }
-          }
-          mx = max_nan(mx, vm);
-          if ((u & (sstride - 1)) == 0) samp[u / sstride] = v[j];
-        }
+        if (u < nvec && (u & (sstride - 1)) == 0) samp[u / sstride] = v[j];
       }
     }
-    const float m_thread = mx;
     mx = warp_max_nan(mx);
     if (lane == 0) sm.redf[warp] = mx;
     for (int j = tid; j <= kFB; j += kTT) {
@@ -893,7 +893,9 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
     // The row's mass relative to M, in fixed point (every thread gets it).
     unsigned long long S = 0, unused0 = 0;
     if (pmass) {
-      const float sc = m_thread > -INFINITY ? s_run * ex2((m_thread - M) * k) : 0.0f;
+      float s0, s1;
+      upk(s_run, s0, s1);
+      const float sc = m_run > -INFINITY ? (s0 + s1) * ex2((m_run - M) * k) : 0.0f;
       S = __float2ull_rn(sc * kFix);
       block_sum2(sm, S, unused0, lane, warp);
     }
