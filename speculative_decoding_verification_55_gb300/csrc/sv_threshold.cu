@@ -186,18 +186,20 @@ __device__ __forceinline__ void class_words(const uint4& v, float xt, float xa, 
   }
 }
 
-// Bit e of the result: logit e's entry of the class words.
+// Bit e of the result: logit e's entry of the class words. bf16: a byte of each half per logit
+// (in logit order, by byte permutes), then one bit of each byte gathered by a multiply (the four
+// partial products land on distinct bits, so nothing carries).
 template <bool BF16>
 __device__ __forceinline__ unsigned word_bits(const uint32_t m[4]) {
+  if (BF16) {
+    const uint32_t lo = __byte_perm(m[0], m[1], 0x6420) & 0x01010101u;   // logits 0..3
+    const uint32_t hi = __byte_perm(m[2], m[3], 0x6420) & 0x01010101u;   // logits 4..7
+    constexpr uint32_t kGather = (1u << 28) | (1u << 21) | (1u << 14) | (1u << 7);
+    return ((lo * kGather) >> 28) | (((hi * kGather) >> 24) & 0xf0u);
+  }
   unsigned bits = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    if (BF16) {
-      bits |= ((m[q] & 1u) | ((m[q] >> 15) & 2u)) << (2 * q);
-    } else {
-      bits |= (m[q] & 1u) << q;
-    }
-  }
+  for (int q = 0; q < 4; ++q) bits |= (m[q] & 1u) << q;
   return bits;
 }
 
@@ -711,6 +713,7 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
   };
   static_assert(kU * E <= 32, "one bit per logit of a step in a word");
   const f32x2 k2 = pk(k, k), c2 = pk(-Mk, -Mk);
+  uint32_t pmx = 0xFF80FF80u;                       // bf16: the running max of both halves (-inf)
   for (int u0 = 0; u0 < nvec; u0 += kTT * kU) {
     uint4 vv[kU];
     load(u0, vv);
@@ -720,7 +723,10 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
       const bool in = u0 + j * kTT + tid < nvec;
       const uint4 v = vv[j];
       uint32_t cw[4], aw[4];
-      if (kMax && in) mx = max_nan(mx, vec_max<BF16>(v));
+      if (kMax && in) {
+        if (BF16) pmx = bmax2_nan(pmx, bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w)));
+        else mx = max_nan(mx, vec_max<BF16>(v));
+      }
       class_words<BF16, kP>(v, xt, xa, xl, cw, aw);
       if (in && (cw[0] | cw[1] | cw[2] | cw[3]) != 0u) bits |= word_bits<BF16>(cw) << (j * E);
       if (kP && in && (aw[0] | aw[1] | aw[2] | aw[3]) != 0u) {
@@ -773,6 +779,7 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
       }
     }
   }
+  if (kMax && BF16) mx = max_nan(mx, max_nan(bf_lo(pmx), bf_hi(pmx)));
   return s_a;
 }
 
