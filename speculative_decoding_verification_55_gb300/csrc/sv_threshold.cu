@@ -41,6 +41,8 @@
 // Within a bin, decisions are on exact keys and integer masses; bins and cut points only choose
 // what is listed (membership is recomputed with the same compares in every pass).
 
+#include <type_traits>
+
 #include "sv_common.cuh"
 
 namespace sv {
@@ -703,24 +705,28 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
                                        uint64_t pol, int tid, int lane, float& mx) {
   constexpr int E = BF16 ? 8 : 4;
   float s_a = 0.0f;
-  auto load = [&](int base, uint4 (&dst)[kU]) {
-#pragma unroll
-    for (int j = 0; j < kU; ++j) {
-      const int u = base + j * kTT + tid;
-      dst[j] = make_uint4(0u, 0u, 0u, 0u);
-      if (u < nvec) dst[j] = ld_pol_v4(rv + u, pol);
-    }
-  };
   static_assert(kU * E <= 32, "one bit per logit of a step in a word");
   const f32x2 k2 = pk(k, k), c2 = pk(-Mk, -Mk);
   uint32_t pmx = 0xFF80FF80u;                       // bf16: the running max of both halves (-inf)
-  for (int u0 = 0; u0 < nvec; u0 += kTT * kU) {
+  // One step of kU vectors per thread; a full step (every vector inside the row, all but the
+  // row's last step) skips the bounds checks.
+  auto step = [&](int u0, auto full_tag) {
+    constexpr bool kAll = decltype(full_tag)::value;
     uint4 vv[kU];
-    load(u0, vv);
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int u = u0 + j * kTT + tid;
+      if (kAll) {
+        vv[j] = ld_pol_v4(rv + u, pol);
+      } else {
+        vv[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (u < nvec) vv[j] = ld_pol_v4(rv + u, pol);
+      }
+    }
     unsigned bits = 0;                              // bit j*E + e: logit e of vector j is a candidate
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
-      const bool in = u0 + j * kTT + tid < nvec;
+      const bool in = kAll || u0 + j * kTT + tid < nvec;
       const uint4 v = vv[j];
       uint32_t cw[4], aw[4];
       if (kMax && in) {
@@ -778,7 +784,10 @@ __device__ __forceinline__ float pass2(TShared& sm, float* cand, int* cidx, cons
         }
       }
     }
-  }
+  };
+  int u0 = 0;
+  for (; u0 + kTT * kU <= nvec; u0 += kTT * kU) step(u0, std::true_type{});
+  if (u0 < nvec) step(u0, std::false_type{});
   if (kMax && BF16) mx = max_nan(mx, max_nan(bf_lo(pmx), bf_hi(pmx)));
   return s_a;
 }
@@ -864,20 +873,27 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
         mx = max_nan(mx, vec_max<BF16>(v));
       }
     }
-    for (int u0 = tid; pmass && u0 < nvec; u0 += kTT * kU) {
+    // Full steps (every vector inside the row) skip the bounds checks.
+    auto mass_step = [&](int u0, auto full_tag) {
+      constexpr bool kAll = decltype(full_tag)::value;
       constexpr uint32_t ninf = BF16 ? 0xFF80FF80u : 0xFF800000u;
       uint4 v[kU];
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int u = u0 + j * kTT;
-        v[j] = u < nvec ? ld_pol_v4(R.rv + u, keep) : make_uint4(ninf, ninf, ninf, ninf);
+        v[j] = (kAll || u < nvec) ? ld_pol_v4(R.rv + u, keep) : make_uint4(ninf, ninf, ninf, ninf);
       }
       online_update_batch<BF16, kU>(v, k, m_run, s_run, mx);
 #pragma unroll
       for (int j = 0; j < kU; ++j) {
         const int u = u0 + j * kTT;
-        if (u < nvec && (u & (sstride - 1)) == 0) samp[u / sstride] = v[j];
+        if ((kAll || u < nvec) && (u & (sstride - 1)) == 0) samp[u / sstride] = v[j];
       }
+    };
+    if (pmass) {
+      int u0 = tid;
+      for (; u0 - tid + kTT * kU <= nvec; u0 += kTT * kU) mass_step(u0, std::true_type{});
+      if (u0 - tid < nvec) mass_step(u0, std::false_type{});
     }
     mx = warp_max_nan(mx);
     if (lane == 0) sm.redf[warp] = mx;
