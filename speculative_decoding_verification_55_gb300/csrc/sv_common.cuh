@@ -444,7 +444,8 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 // Inner loops over 16-byte vectors of logits (8 bf16 or 4 fp32)
 // ------------------------------------------------------------------------------------------------
 
-// Pass-1 update with the N vectors one thread takes from a ring slot: one max and one
+// Online softmax update with N vectors of one thread (a ring slot's share in the streaming
+// kernel's pass 1, a step of a top-p row's first pass in the threshold kernel): one max and one
 // rescale check for the batch, then every exp2 with two independent accumulators.
 template <bool BF16, int N>
 __device__ __forceinline__ void online_update_batch(const uint4 (&v)[N], float k, float& m, f32x2& s,
