@@ -120,6 +120,13 @@ __device__ __forceinline__ int d_bin(float z, float Mk, float k, float per, int 
 
 // Mass of a logit relative to the max, 2^-d, in fixed point; at most 1 (the max's own mass, which
 // the rounding of M k can push a little above 1), so V masses sum below 2^64 for V < 2^22.
+// An approximate square root (the hardware's, not correctly rounded).
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ unsigned long long fix_mass(float z, float Mk, float k) {
   const float w = fminf(ex2(fmaf(z, k, -Mk)), 1.0f);
   return __float2ull_rn(w * kFix);
@@ -997,19 +1004,21 @@ __global__ void __launch_bounds__(kTT, kCtasT) sv_threshold_kernel(const Params 
         }
         // Variances: f (f - 1) times the sample's squared masses.
         const float ffk = f * (f - 1.0f);
+        // est_above(b) and 5 sd(b) from the sample masses of the bins >= b, once per bin (the
+        // margin needs no correctly rounded square root). Bin b decides b_c with its own pair and
+        // b_lo for bin b - 1.
         int bc_l = -1, blo_l = kFB;
         float sb = sfx, sb2 = sfx2;                  // sample mass of bins >= lane * 16 + i2
-        for (int i2 = 0; i2 < 16; ++i2) {
+        for (int i2 = 0; i2 <= 16; ++i2) {
           const int bb = lane * 16 + i2;
-          const float ea = Sf - f * sb;
-          const float sd = 5.0f * sqrtf(ffk * fmaxf(sb2, 0.0f));
+          const float ea = Sf - f * fmaxf(sb, 0.0f);
+          const float sd = 5.0f * sqrt_approx(ffk * fmaxf(sb2, 0.0f));
+          if (i2 > 0 && blo_l == kFB && ea - sd >= target) blo_l = bb - 1;   // bins <= bb - 1 reach it
+          if (i2 == 16) break;
           if (ea + sd <= target) bc_l = bb;          // A = bins < bb stays below the target
           const float mb = bin_mass(bb);
           sb -= mb;
           sb2 -= mb * ex2(-static_cast<float>(bb) / kFBPerLog2);
-          const float ea1 = Sf - f * fmaxf(sb, 0.0f);
-          const float sd1 = 5.0f * sqrtf(ffk * fmaxf(sb2, 0.0f));
-          if (blo_l == kFB && ea1 - sd1 >= target) blo_l = bb;   // bins <= bb reach it
         }
         const unsigned hc = __ballot_sync(kFull, bc_l >= 0);
         b_c = hc ? __shfl_sync(kFull, bc_l, 31 - __clz(hc)) : 0;
